@@ -1,0 +1,163 @@
+/*
+ * kpool.h -- C ABI of the GB300 (sm_103a) KPool DSA indexer selection library.
+ *
+ * The operation (per packed batch of causal sequences):
+ *   1. Mean-pool every kpool consecutive index keys of a sequence into one pooled
+ *      key ("spark_model/layers/glm5next_dsa/tp.rs", module docs, "Why the
+ *      indexer is REPLICATED": n_pools = seq / kpool). The pages do not name the
+ *      pooling operator; this library reads it as the mean: an fp32 sum in key
+ *      order, an IEEE fp32 division by kpool, round-to-nearest-even to the input
+ *      dtype.
+ *   2. Score every causally eligible (query row t, pool p) pair,
+ *         s[t,p] = sum_h w[t,h] * relu(scale * q[t,h,:] . kpool[p,:]),
+ *      a plain sum over heads taken before any top-k (same page and section).
+ *      A row t (sequence-local) may use the pools p < floor((t+1)/kpool), i.e.
+ *      the complete pools whose last key is at or before t.
+ *   3. Keep the top budget = index_topk / kpool pools of each row, ordered by
+ *      higher score first and then smaller pool index (tp.rs module docs: the
+ *      deterministic tiebreak pinned because torch.topk's tie order is
+ *      undefined). Rows with fewer eligible pools are padded with -1.
+ *   4. Expand the chosen pools to token ids, append the row's own incomplete
+ *      trailing pool and apply the causal / varlen mask ("NVIDIA/Megatron-LM
+ *      pull request #8299", section "Change": pool expansion, tail append and
+ *      mask filtering run on the [batch, sq, budget] pool ids).
+ *
+ * Sequences arrive packed (THD) with cumulative lengths cu_seqlens, as in the
+ * pages' packed-THD tests (Megatron-LM #8299, section "Test plan"); a dense
+ * batch [B, sq] is cu_seqlens = {0, sq, 2sq, ...}. Every index the library
+ * returns is sequence-local.
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory. Scratch state lives in a caller-provided
+ *     workspace of kpool_workspace_bytes() bytes (256-byte aligned).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). The returned status covers host-side validation and launch
+ *     errors; errors found on the device (malformed cu_seqlens, a bounded wait
+ *     that ran out) are recorded in the workspace and read back with
+ *     kpool_last_device_error().
+ *   - Validation happens before anything touches the GPU: a call that returns
+ *     KPOOL_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE launched nothing.
+ *   - Calls that share a workspace must not overlap on the GPU.
+ *
+ * Layouts (row-major, contiguous):
+ *   q          [T, H, d]            dtype   (16-byte aligned)
+ *   k          [T, d]               dtype   (16-byte aligned)
+ *   w          [T, H]               fp32
+ *   cu_seqlens [S + 1]              int32   cu[0] = 0, nondecreasing, cu[S] = T
+ *   pool ids   [T, budget]          int32   rank order, -1 padded
+ *   token ids  [T, index_topk+kpool] int32  slot j*kpool + r = pool_ids[j]*kpool + r;
+ *                                           slots index_topk + r = the row's tail;
+ *                                           -1 where empty or masked
+ *   pool scores[T, budget]          fp32    score of each chosen pool, -INFINITY on -1 slots
+ */
+#ifndef KPOOL_H_
+#define KPOOL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KPOOL_OK = 0,
+  KPOOL_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, kpool < 1,
+                                   index_topk % kpool != 0, malformed cu_seqlens */
+  KPOOL_ERR_UNSUPPORTED = 2,    /* shape outside what the kernels implement */
+  KPOOL_ERR_WORKSPACE = 3,      /* workspace null, misaligned or too small */
+  KPOOL_ERR_CUDA = 4,           /* a CUDA runtime/driver call or launch failed */
+  KPOOL_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait ran out */
+} kpool_status;
+
+typedef enum { KPOOL_BF16 = 0, KPOOL_F32 = 1 } kpool_dtype;
+
+/* Which score+select kernel kpool_select_ex runs. */
+typedef enum {
+  KPOOL_SCORE_AUTO = 0,   /* tensor-core kernel when the shape allows, else SIMT */
+  KPOOL_SCORE_TC = 1,     /* tcgen05/TMEM kernel: bf16, H = 32, d = 128, budget <= 512 */
+  KPOOL_SCORE_SIMT = 2    /* CUDA-core kernel: any H <= 64, d <= 256, budget <= 4096 */
+} kpool_score_kernel;
+
+typedef struct {
+  int32_t score_kernel;   /* a kpool_score_kernel value */
+  int32_t max_ctas;       /* 0: one persistent CTA per SM; > 0: cap (tests vary it) */
+  int32_t reserved[6];    /* must be zero */
+} kpool_options;
+
+/*
+ * Workspace size, in bytes, for a call with these sizes. Pure host arithmetic;
+ * never touches the GPU. Returns 0 for arguments kpool_select would reject.
+ */
+size_t kpool_workspace_bytes(int64_t total_tokens, int32_t num_seqs, int32_t heads, int32_t head_dim,
+                             kpool_dtype dtype, int32_t kpool, int32_t index_topk);
+
+/*
+ * The whole selection (steps 1-4 above) for one packed batch.
+ *   q, k, w, cu_seqlens  inputs as laid out above (device).
+ *   scale                the fp32 factor inside the relu (any finite value).
+ *   out_pool_ids         [T, budget] int32 (device), written for every row.
+ *   out_token_ids        [T, index_topk + kpool] int32 (device), written for every row.
+ *   out_pool_scores      [T, budget] fp32 (device) or NULL.
+ *   workspace            device scratch of >= kpool_workspace_bytes(...) bytes.
+ * T = 0 is a valid no-op. Requires d % 8 == 0 (16-byte rows) and heads >= 1.
+ */
+kpool_status kpool_select(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
+                          int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                          kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                          int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* kpool_select with explicit options (NULL = defaults). */
+kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
+                             int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                             kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                             int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             const kpool_options* options);
+
+/*
+ * Step 1 alone: writes the pooled keys [P, d] (dtype, P = sum_b floor(L_b/kpool),
+ * sequences back to back) to out_pooled_keys, which must hold
+ * floor(T/kpool) * d elements. Uses the workspace for the per-sequence offsets.
+ */
+kpool_status kpool_pool_keys(const void* k, const int32_t* cu_seqlens, int32_t num_seqs,
+                             int64_t total_tokens, int32_t head_dim, kpool_dtype dtype, int32_t kpool,
+                             void* out_pooled_keys, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Step 4 alone: expands pool ids [T, budget] (as kpool_select writes them) into
+ * token ids [T, index_topk + kpool], appending each row's tail and applying the
+ * causal/varlen mask. Ids outside [0, floor((t+1)/kpool)) are treated as -1.
+ */
+kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, int32_t num_seqs,
+                          int64_t total_tokens, int32_t kpool, int32_t index_topk,
+                          int32_t* out_token_ids, void* stream);
+
+/*
+ * Synchronises `stream`, then reads the device error word the last call on this
+ * workspace recorded: KPOOL_OK, KPOOL_ERR_INVALID_ARG (malformed cu_seqlens),
+ * KPOOL_ERR_DEVICE_TIMEOUT (a bounded wait ran out), or KPOOL_ERR_CUDA if the
+ * synchronisation or copy itself failed.
+ */
+kpool_status kpool_last_device_error(const void* workspace, void* stream);
+
+/*
+ * Exercises the bounded device-side wait used by the pipelined kernel: one CTA
+ * waits on a barrier that nothing ever completes, gives up after
+ * `spin_limit` polls, records KPOOL_ERR_DEVICE_TIMEOUT in the workspace error
+ * word and returns. No fault, trap or hang is involved. Asynchronous; read the
+ * result with kpool_last_device_error().
+ */
+kpool_status kpool_wait_timeout_selftest(void* workspace, size_t workspace_bytes, int64_t spin_limit,
+                                         void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* kpool_status_string(kpool_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KPOOL_H_ */

@@ -1,0 +1,240 @@
+// kpool_api.cu -- the C ABI declared in include/kpool.h: argument validation,
+// workspace carve-up and the launch sequence K0 plan -> K1 pool -> K2 score +
+// select -> K3 expand on the caller's stream. Nothing here allocates device
+// memory or synchronises, except kpool_last_device_error (documented to sync).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kpool_internal.cuh"
+#include "kpool_ptx.cuh"
+
+namespace kpool {
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+
+cudaError_t sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && g_sm_count[dev] > 0) {
+    *out = g_sm_count[dev];
+    return cudaSuccess;
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev] = n;
+  *out = n;
+  return cudaSuccess;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t elem_bytes(kpool_dtype dt) { return dt == KPOOL_BF16 ? 2 : 4; }
+
+// Shape checks shared by every entry point; pointer checks are per entry point.
+kpool_status check_shape(int64_t T, int32_t S, int32_t d, kpool_dtype dtype, int32_t kpool) {
+  if (T < 0 || T > int64_t(INT32_MAX)) return KPOOL_ERR_INVALID_ARG;
+  if (S < 0 || (T > 0 && S < 1)) return KPOOL_ERR_INVALID_ARG;
+  if (dtype != KPOOL_BF16 && dtype != KPOOL_F32) return KPOOL_ERR_INVALID_ARG;
+  if (kpool < 1 || d < 1) return KPOOL_ERR_INVALID_ARG;
+  if ((size_t(d) * elem_bytes(dtype)) % 16 != 0) return KPOOL_ERR_INVALID_ARG;  // 16-byte rows
+  return KPOOL_OK;
+}
+
+kpool_status check_workspace(const void* ws, size_t bytes, const WorkspaceLayout& L) {
+  if (ws == nullptr || !aligned(ws, 256) || bytes < L.total) return KPOOL_ERR_WORKSPACE;
+  return KPOOL_OK;
+}
+
+__global__ void wait_selftest_kernel(WorkspaceHeader* hdr, int64_t spin_limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  hdr->error = 0;
+  ptx::mbar_init(&bar, 1);
+  ptx::fence_mbar_init();
+  // Nothing ever arrives on `bar`: the bounded wait must give up by itself.
+  if (!ptx::mbar_wait_bounded(&bar, 0, spin_limit, 1000000000ull)) record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(char* ws, int64_t spin_limit, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<WorkspaceHeader*>(ws), spin_limit);
+  return cudaGetLastError();
+}
+
+}  // namespace kpool
+
+using namespace kpool;
+
+extern "C" {
+
+size_t kpool_workspace_bytes(int64_t total_tokens, int32_t num_seqs, int32_t heads, int32_t head_dim,
+                             kpool_dtype dtype, int32_t kpool, int32_t index_topk) {
+  if (check_shape(total_tokens, num_seqs, head_dim, dtype, kpool) != KPOOL_OK) return 0;
+  if (heads < 1 || index_topk < 0 || index_topk % kpool != 0) return 0;
+  return workspace_layout(total_tokens, num_seqs, head_dim, elem_bytes(dtype), kpool).total;
+}
+
+kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
+                             int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                             kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                             int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                             void* workspace, size_t workspace_bytes, void* stream_ptr,
+                             const kpool_options* options) {
+  kpool_options opt{};
+  if (options) opt = *options;
+  for (int i = 0; i < 6; ++i)
+    if (opt.reserved[i] != 0) return KPOOL_ERR_INVALID_ARG;
+  if (opt.score_kernel < KPOOL_SCORE_AUTO || opt.score_kernel > KPOOL_SCORE_SIMT || opt.max_ctas < 0)
+    return KPOOL_ERR_INVALID_ARG;
+
+  kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
+  if (st != KPOOL_OK) return st;
+  if (heads < 1 || index_topk < 0 || index_topk % kpool != 0 || !isfinite(scale)) return KPOOL_ERR_INVALID_ARG;
+  const int32_t budget = index_topk / kpool;
+  const int64_t T = total_tokens;
+  if (T == 0) return KPOOL_OK;
+  if (!q || !k || !w || !cu_seqlens || !out_token_ids || (budget > 0 && !out_pool_ids))
+    return KPOOL_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 4) || !aligned(cu_seqlens, 4) ||
+      !aligned(out_pool_ids, 4) || !aligned(out_token_ids, 4) || !aligned(out_pool_scores, 4))
+    return KPOOL_ERR_INVALID_ARG;
+
+  const bool tc_ok = select_tc_supported(dtype, heads, head_dim, budget);
+  const bool simt_ok = heads <= 64 && head_dim <= 256 && budget <= 4096;
+  bool use_tc;
+  switch (opt.score_kernel) {
+    case KPOOL_SCORE_TC:
+      if (!tc_ok) return KPOOL_ERR_UNSUPPORTED;
+      use_tc = true;
+      break;
+    case KPOOL_SCORE_SIMT:
+      if (!simt_ok) return KPOOL_ERR_UNSUPPORTED;
+      use_tc = false;
+      break;
+    default:
+      if (!tc_ok && !simt_ok) return KPOOL_ERR_UNSUPPORTED;
+      use_tc = tc_ok;
+  }
+
+  const WorkspaceLayout L = workspace_layout(T, num_seqs, head_dim, elem_bytes(dtype), kpool);
+  st = check_workspace(workspace, workspace_bytes, L);
+  if (st != KPOOL_OK) return st;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int sms = 0;
+  if (sm_count(&sms) != cudaSuccess) return KPOOL_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  void* pooled = ws + L.pooled;
+
+  if (launch_plan(cu_seqlens, num_seqs, T, kpool, ws, L, stream) != cudaSuccess) return KPOOL_ERR_CUDA;
+  if (launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, pooled, ws, L, sms, stream) != cudaSuccess)
+    return KPOOL_ERR_CUDA;
+  if (budget > 0) {
+    cudaError_t e;
+    if (use_tc) {
+      int grid = sms;
+      if (opt.max_ctas > 0 && opt.max_ctas < grid) grid = opt.max_ctas;
+      e = launch_select_tc(q, pooled, w, cu_seqlens, num_seqs, T, kpool, budget, scale, out_pool_ids,
+                           out_pool_scores, ws, L, grid, stream);
+    } else {
+      e = launch_select_simt(q, pooled, w, dtype, cu_seqlens, num_seqs, T, heads, head_dim, kpool, budget, scale,
+                             out_pool_ids, out_pool_scores, ws, L, opt.max_ctas > 0 ? opt.max_ctas : sms, stream);
+    }
+    if (e != cudaSuccess) return KPOOL_ERR_CUDA;
+  }
+  if (launch_expand(out_pool_ids, cu_seqlens, num_seqs, T, kpool, budget, out_token_ids,
+                    reinterpret_cast<const WorkspaceHeader*>(ws + L.header), sms, stream) != cudaSuccess)
+    return KPOOL_ERR_CUDA;
+  return KPOOL_OK;
+}
+
+kpool_status kpool_select(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
+                          int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                          kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                          int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return kpool_select_ex(q, k, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool, index_topk,
+                         scale, out_pool_ids, out_token_ids, out_pool_scores, workspace, workspace_bytes, stream,
+                         nullptr);
+}
+
+kpool_status kpool_pool_keys(const void* k, const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                             int32_t head_dim, kpool_dtype dtype, int32_t kpool, void* out_pooled_keys,
+                             void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
+  if (st != KPOOL_OK) return st;
+  if (total_tokens == 0) return KPOOL_OK;
+  if (!k || !cu_seqlens || (total_tokens / kpool > 0 && !out_pooled_keys)) return KPOOL_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(out_pooled_keys, 16) || !aligned(cu_seqlens, 4)) return KPOOL_ERR_INVALID_ARG;
+  const WorkspaceLayout L = workspace_layout(total_tokens, num_seqs, head_dim, elem_bytes(dtype), kpool);
+  st = check_workspace(workspace, workspace_bytes, L);
+  if (st != KPOOL_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int sms = 0;
+  if (sm_count(&sms) != cudaSuccess) return KPOOL_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  if (launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, ws, L, stream) != cudaSuccess) return KPOOL_ERR_CUDA;
+  if (launch_pool(k, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool, out_pooled_keys, ws, L, sms,
+                  stream) != cudaSuccess)
+    return KPOOL_ERR_CUDA;
+  return KPOOL_OK;
+}
+
+kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, int32_t num_seqs,
+                          int64_t total_tokens, int32_t kpool, int32_t index_topk, int32_t* out_token_ids,
+                          void* stream_ptr) {
+  if (total_tokens < 0 || total_tokens > int64_t(INT32_MAX) || num_seqs < 0 || (total_tokens > 0 && num_seqs < 1))
+    return KPOOL_ERR_INVALID_ARG;
+  if (kpool < 1 || index_topk < 0 || index_topk % kpool != 0) return KPOOL_ERR_INVALID_ARG;
+  if (total_tokens == 0) return KPOOL_OK;
+  const int32_t budget = index_topk / kpool;
+  if (!cu_seqlens || !out_token_ids || (budget > 0 && !pool_ids)) return KPOOL_ERR_INVALID_ARG;
+  if (!aligned(pool_ids, 4) || !aligned(out_token_ids, 4) || !aligned(cu_seqlens, 4)) return KPOOL_ERR_INVALID_ARG;
+  int sms = 0;
+  if (sm_count(&sms) != cudaSuccess) return KPOOL_ERR_CUDA;
+  if (launch_expand(pool_ids, cu_seqlens, num_seqs, total_tokens, kpool, budget, out_token_ids, nullptr, sms,
+                    static_cast<cudaStream_t>(stream_ptr)) != cudaSuccess)
+    return KPOOL_ERR_CUDA;
+  return KPOOL_OK;
+}
+
+kpool_status kpool_last_device_error(const void* workspace, void* stream_ptr) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return KPOOL_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KPOOL_ERR_CUDA;
+  int32_t code = 0;
+  if (cudaMemcpy(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return KPOOL_ERR_CUDA;
+  if (code < 0 || code > KPOOL_ERR_DEVICE_TIMEOUT) return KPOOL_ERR_CUDA;
+  return static_cast<kpool_status>(code);
+}
+
+kpool_status kpool_wait_timeout_selftest(void* workspace, size_t workspace_bytes, int64_t spin_limit,
+                                         void* stream_ptr) {
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < sizeof(WorkspaceHeader))
+    return KPOOL_ERR_WORKSPACE;
+  if (spin_limit < 1) return KPOOL_ERR_INVALID_ARG;
+  if (launch_wait_selftest(static_cast<char*>(workspace), spin_limit, static_cast<cudaStream_t>(stream_ptr)) !=
+      cudaSuccess)
+    return KPOOL_ERR_CUDA;
+  return KPOOL_OK;
+}
+
+const char* kpool_status_string(kpool_status status) {
+  switch (status) {
+    case KPOOL_OK: return "ok";
+    case KPOOL_ERR_INVALID_ARG: return "invalid argument";
+    case KPOOL_ERR_UNSUPPORTED: return "unsupported shape";
+    case KPOOL_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case KPOOL_ERR_CUDA: return "CUDA error";
+    case KPOOL_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

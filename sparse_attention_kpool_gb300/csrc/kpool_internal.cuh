@@ -1,0 +1,126 @@
+// kpool_internal.cuh -- shared pieces of the CUDA library: workspace layout,
+// the ordered selection key, and the launch wrappers each .cu file provides.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kpool.h"
+
+namespace kpool {
+
+// Query rows handled together by one work item of the tensor-core kernel
+// (8 rows x 32 heads = 256 MMA columns).
+constexpr int kItemRows = 8;
+
+// ---------------------------------------------------------------- workspace
+//
+// [header 256 B][pool_off S+1][qblk_off S+1][level_cnt L][level_start L]
+// [level_fill L][items N x int2][pooled keys P x d]; every region 256-B aligned.
+struct WorkspaceHeader {
+  int32_t error;        // kpool_status recorded on the device (0 = OK)
+  int32_t n_items;      // work items written by the planning kernel
+  int32_t n_levels;     // distinct item depths
+  int32_t total_pools;  // P
+  int32_t reserved[60];
+};
+static_assert(sizeof(WorkspaceHeader) == 256, "header is one 256-byte block");
+
+struct WorkspaceLayout {
+  size_t header, pool_off, qblk_off, level_cnt, level_start, level_fill, items, pooled, total;
+  int64_t max_items, max_levels, max_pools;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WorkspaceLayout workspace_layout(int64_t T, int32_t S, int32_t d, size_t elem_bytes, int32_t kpool) {
+  WorkspaceLayout L{};
+  L.max_items = (T + kItemRows - 1) / kItemRows + S + 1;
+  L.max_levels = (T + kItemRows - 1) / kItemRows + 2;
+  L.max_pools = T / kpool;
+  size_t off = 0;
+  L.header = off;      off = align256(off + sizeof(WorkspaceHeader));
+  L.pool_off = off;    off = align256(off + sizeof(int32_t) * size_t(S + 1));
+  L.qblk_off = off;    off = align256(off + sizeof(int32_t) * size_t(S + 1));
+  L.level_cnt = off;   off = align256(off + sizeof(int32_t) * size_t(L.max_levels));
+  L.level_start = off; off = align256(off + sizeof(int32_t) * size_t(L.max_levels));
+  L.level_fill = off;  off = align256(off + sizeof(int32_t) * size_t(L.max_levels));
+  L.items = off;       off = align256(off + sizeof(int2) * size_t(L.max_items));
+  L.pooled = off;      off = align256(off + elem_bytes * size_t(d) * size_t(L.max_pools > 0 ? L.max_pools : 1));
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------ selection key
+//
+// A 64-bit key whose unsigned order is the selection order: the high word is
+// the score mapped to an order-preserving unsigned integer, the low word is
+// the bitwise complement of the pool index (so a smaller index ranks higher on
+// equal scores). -0 is folded into +0 first, so the two zeros tie. Finite
+// scores never produce the key 0, which therefore marks an empty slot.
+__device__ __forceinline__ uint64_t make_key(float s, uint32_t pool) {
+  s = (s == 0.0f) ? 0.0f : s;
+  uint32_t u = __float_as_uint(s);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (uint64_t(u) << 32) | uint64_t(~pool);
+}
+
+__device__ __forceinline__ uint32_t key_pool(uint64_t key) { return ~uint32_t(key); }
+
+__device__ __forceinline__ float key_score(uint64_t key) {
+  uint32_t u = uint32_t(key >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+// Sequence holding global row `row` (cu is nondecreasing, row < cu[S]).
+__device__ __forceinline__ int seq_of_row(const int32_t* cu, int S, int64_t row) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (int64_t(__ldg(cu + mid)) <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void record_error(WorkspaceHeader* hdr, int code) {
+  atomicCAS(&hdr->error, 0, code);
+}
+
+// ------------------------------------------------------ launch wrappers
+// Each returns cudaGetLastError() after enqueueing its kernel on `stream`.
+
+// K0: validates cu_seqlens, writes pool/item offsets and the heavy-first item
+// list; clears the header. One CTA.
+cudaError_t launch_plan(const int32_t* cu, int32_t S, int64_t T, int32_t kpool, char* ws,
+                        const WorkspaceLayout& L, cudaStream_t stream);
+
+// K1: pooled keys [P, d] into `out` (dtype elements).
+cudaError_t launch_pool(const void* k, kpool_dtype dtype, const int32_t* cu, int32_t S, int64_t T,
+                        int32_t d, int32_t kpool, void* out, const char* ws, const WorkspaceLayout& L,
+                        int num_sms, cudaStream_t stream);
+
+// K2 (CUDA cores): any supported shape.
+cudaError_t launch_select_simt(const void* q, const void* kp, const float* w, kpool_dtype dtype,
+                               const int32_t* cu, int32_t S, int64_t T, int32_t H, int32_t d, int32_t kpool,
+                               int32_t budget, float scale, int32_t* out_ids, float* out_scores,
+                               char* ws, const WorkspaceLayout& L, int num_sms, cudaStream_t stream);
+
+// K2 (tensor cores): bf16, H = 32, d = 128, budget <= 512.
+bool select_tc_supported(kpool_dtype dtype, int32_t H, int32_t d, int32_t budget);
+cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, const int32_t* cu, int32_t S,
+                             int64_t T, int32_t kpool, int32_t budget, float scale, int32_t* out_ids,
+                             float* out_scores, char* ws, const WorkspaceLayout& L, int grid,
+                             cudaStream_t stream);
+
+// K3: pool ids -> token ids.
+// `hdr` may be null; when given, the kernel does nothing if the planning
+// kernel recorded an error.
+cudaError_t launch_expand(const int32_t* pool_ids, const int32_t* cu, int32_t S, int64_t T, int32_t kpool,
+                          int32_t budget, int32_t* out_tokens, const WorkspaceHeader* hdr, int num_sms,
+                          cudaStream_t stream);
+
+// Bounded-wait self test.
+cudaError_t launch_wait_selftest(char* ws, int64_t spin_limit, cudaStream_t stream);
+
+}  // namespace kpool

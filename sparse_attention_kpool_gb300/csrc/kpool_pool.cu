@@ -1,0 +1,115 @@
+// kpool_pool.cu -- K1: mean-pooling of index keys.
+//
+// kp[pool_off[b] + p, c] = round_to_dtype( (sum_{j<kpool} k[cu[b] + p*kpool + j, c]) / kpool )
+// The pages group kpool consecutive index keys into one pool ("spark_model/
+// layers/glm5next_dsa/tp.rs", module docs: n_pools = seq / kpool) but never
+// name the operator; the mean is this library's stated reading. The sum runs in
+// fp32 in key order, the division is IEEE-rounded, the result is rounded to
+// nearest even in the input dtype -- so a bf16 MMA consumes it exactly.
+//
+// HBM-bound: each thread owns one 16-byte chunk (8 bf16 / 4 fp32 channels) of
+// one pooled row, reads kpool 16-byte vectors (coalesced across the chunk
+// threads of a row) and writes one. Grid-stride over P * d/vec chunks.
+#include <cuda_bf16.h>
+
+#include "kpool_internal.cuh"
+
+namespace kpool {
+namespace {
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int kLanes = 8;
+};
+template <>
+struct Vec<float> {
+  static constexpr int kLanes = 4;
+};
+
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8], __nv_bfloat16*) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 x = __bfloat1622float2(h[i]);
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8], float*) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[8], __nv_bfloat16*) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[8], float*) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) pool_kernel(const T* __restrict__ k, const int32_t* __restrict__ cu,
+                                                   const int32_t* __restrict__ pool_off,
+                                                   const WorkspaceHeader* __restrict__ hdr, int S, int d,
+                                                   int kpool, T* __restrict__ out) {
+  constexpr int V = Vec<T>::kLanes;
+  if (hdr->error != 0) return;
+  const int64_t P = hdr->total_pools;
+  const int chunks = d / V;
+  const int64_t total = P * chunks;
+  const float divisor = float(kpool);
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t g = i / chunks;  // global pool row
+    const int c = int(i - g * chunks) * V;
+    // sequence of pool g: last b with pool_off[b] <= g
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (int64_t(__ldg(pool_off + mid)) <= g) lo = mid; else hi = mid - 1;
+    }
+    const int64_t p = g - __ldg(pool_off + lo);
+    const int64_t first = int64_t(__ldg(cu + lo)) + p * kpool;
+    float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    for (int j = 0; j < kpool; ++j) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(k + (first + j) * d + c));
+      float f[8];
+      unpack(v, f, static_cast<T*>(nullptr));
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = __fdiv_rn(acc[e], divisor);
+    *reinterpret_cast<uint4*>(out + g * d + c) = pack(acc, static_cast<T*>(nullptr));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pool(const void* k, kpool_dtype dtype, const int32_t* cu, int32_t S, int64_t T, int32_t d,
+                        int32_t kpool, void* out, const char* ws, const WorkspaceLayout& L, int num_sms,
+                        cudaStream_t stream) {
+  const int64_t max_chunks = (T / kpool) * (d / (dtype == KPOOL_BF16 ? 8 : 4));
+  if (max_chunks == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (max_chunks + threads - 1) / threads;
+  const int64_t cap = int64_t(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  const auto* hdr = reinterpret_cast<const WorkspaceHeader*>(ws + L.header);
+  const auto* pool_off = reinterpret_cast<const int32_t*>(ws + L.pool_off);
+  if (dtype == KPOOL_BF16)
+    pool_kernel<__nv_bfloat16><<<unsigned(blocks), threads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(k), cu, pool_off, hdr, S, d, kpool, static_cast<__nv_bfloat16*>(out));
+  else
+    pool_kernel<float><<<unsigned(blocks), threads, 0, stream>>>(static_cast<const float*>(k), cu, pool_off, hdr,
+                                                                 S, d, kpool, static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace kpool

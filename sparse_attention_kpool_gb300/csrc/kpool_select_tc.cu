@@ -1,0 +1,545 @@
+// kpool_select_tc.cu -- K2 on the 5th-generation tensor cores: fused score +
+// streaming top-budget selection for bf16 inputs, 32 index heads, d = 128.
+//
+// What it computes, per query row t (sequence-local) and eligible pool
+// p < floor((t+1)/kpool):
+//   s[t,p] = sum_h w[t,h] * relu(scale * q[t,h,:] . kp[p,:])
+// ("spark_model/layers/glm5next_dsa/tp.rs", module docs: index_scores
+// accumulates weights[h] * relu(scale . dot) as a plain sum over heads, before
+// any top-k), then the top budget = index_topk/kpool pools of the row under
+// "higher score, then smaller pool index" (same page: the deterministic
+// tiebreak). Every query scores every eligible pool, as on the pages ("NVIDIA/
+// Megatron-LM pull request #8299", "What does this PR do": O(queries x pools)),
+// but only the causally eligible tiles are visited and the [rows, pools] score
+// matrix never leaves the SM.
+//
+// Work item = 8 consecutive query rows of one sequence (the planning kernel
+// lists them deepest-first). Per item the dot products form one dense
+// contraction per tile of 128 pools:
+//   D[p, (t,h)] = kp[p,:] . q[t,h,:]     M = 128 pools, N = 8 rows x 32 heads = 256, K = 128
+// issued as 8 tcgen05.mma (K = 16 each) with bf16 operands staged by TMA in
+// 128-byte-swizzled shared memory and an fp32 accumulator in TMEM. Pools sit on
+// the M axis (TMEM lanes) so each epilogue thread owns one pool and sums the 32
+// heads of a query inside its own registers -- no shuffles.
+//
+// Warp roles (10 warps, one CTA per SM, persistent):
+//   warp 0      TMA producer: the item's q tile (64 KB), then pool tiles into a
+//               3-stage ring (32 KB each).
+//   warp 1      TMEM owner and MMA issuer: two 256-column accumulators, so the
+//               epilogue drains one while the tensor core fills the other.
+//   warps 2..9  epilogue, two groups of four warps (queries 0-3 and 4-7 of the
+//               item); warp w reads TMEM lanes 32*(w%4).. (the hardware rule).
+//               tcgen05.ld -> relu, |scale|*w, head sum in fp32 -> selection key
+//               -> threshold filter -> candidate buffer in shared memory.
+// Selection: 1024 candidate slots per query row. A key enters only if it beats
+// the row's threshold (the budget-th best key kept so far). When a buffer passes
+// 896 entries the owning warp sorts it and cuts it back to `budget`, raising the
+// threshold. After the last tile it sorts once more and writes the ranked ids.
+//
+// Every mbarrier wait is bounded (poll count and ~1 s of wall time). A wait that
+// runs out records KPOOL_ERR_DEVICE_TIMEOUT in the workspace header; all roles
+// then leave their loops through the same barriers, drain their in-flight copies
+// and MMAs, and the TMEM owner frees TMEM before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "kpool_internal.cuh"
+#include "kpool_ptx.cuh"
+
+namespace kpool {
+namespace {
+
+constexpr int kHeads = 32;
+constexpr int kDim = 128;
+constexpr int kRows = kItemRows;          // query rows per item
+constexpr int kN = kRows * kHeads;        // 256 MMA columns
+constexpr int kTilePools = 128;           // MMA M
+constexpr int kStages = 3;
+constexpr int kCap = 1024;                // candidate slots per query row
+constexpr int kMaxBudget = 512;
+constexpr int kCompactAt = kCap - kTilePools;
+constexpr int kThreads = 320;
+constexpr int kAccCols = 256;
+constexpr int kTmemCols = 512;
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t kQHalfBytes = kN * 128;                  // 256 rows x 64 bf16
+constexpr uint32_t kQBytes = 2 * kQHalfBytes;               // 64 KB
+constexpr uint32_t kPoolHalfBytes = kTilePools * 128;       // 128 rows x 64 bf16
+constexpr uint32_t kStageBytes = 2 * kPoolHalfBytes;        // 32 KB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffPool = kOffQ + kQBytes;
+constexpr uint32_t kOffCand = kOffPool + kStages * kStageBytes;
+constexpr uint32_t kOffW = kOffCand + kRows * kCap * 8;
+constexpr uint32_t kOffBar = kOffW + kRows * kHeads * 4;
+constexpr int kNumBars = 2 + 2 * kStages + 4 + 1;
+constexpr uint32_t kOffCount = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffTau = (kOffCount + kRows * 4 + 7) & ~7u;
+constexpr uint32_t kOffElig = kOffTau + kRows * 8;
+constexpr uint32_t kOffMisc = kOffElig + kRows * 4;
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+
+constexpr int64_t kMaxPolls = int64_t(1) << 40;
+constexpr uint64_t kMaxWaitNs = 1000000000ull;  // 1 s; legitimate waits are microseconds
+
+struct Bars {
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* full;       // [kStages]
+  uint64_t* empty;      // [kStages]
+  uint64_t* acc_full;   // [2]
+  uint64_t* acc_empty;  // [2]
+  uint64_t* mma_done;
+};
+
+__device__ __forceinline__ Bars bars_at(uint8_t* base) {
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + kOffBar);
+  Bars r;
+  r.q_full = b + 0;
+  r.q_empty = b + 1;
+  r.full = b + 2;
+  r.empty = b + 2 + kStages;
+  r.acc_full = b + 2 + 2 * kStages;
+  r.acc_empty = b + 4 + 2 * kStages;
+  r.mma_done = b + 6 + 2 * kStages;
+  return r;
+}
+
+// Non-.aligned barrier forms: a warp may arrive with its lanes diverged (the
+// producer and MMA warps do their work on lane 0 only).
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also ORs a flag over the participating threads, so a
+// decision taken after it is the same in every participating warp.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool flag) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "barrier.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(id), "r"(count), "r"(flag ? 1u : 0u)
+      : "memory");
+  return out != 0;
+}
+
+struct Item {
+  int64_t seq_start;  // global row of the sequence's first token
+  int32_t len;        // sequence length
+  int32_t t0;         // first local row of the item
+  int32_t rows;       // valid rows in the item (<= kRows)
+  int32_t pool_base;  // global pooled-key row of the sequence's pool 0
+  int32_t n_tiles;    // pool tiles covering the last row's eligible pools
+};
+
+__device__ __forceinline__ int item_index(int r, int cta, int grid) {
+  return r * grid + ((r & 1) ? (grid - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ Item load_item(const int2* items, const int32_t* cu, const int32_t* pool_off, int idx,
+                                          int kpool) {
+  const int2 it = items[idx];
+  Item m;
+  m.seq_start = cu[it.x];
+  m.len = cu[it.x + 1] - cu[it.x];
+  m.t0 = it.y * kRows;
+  m.rows = min(kRows, m.len - m.t0);
+  m.pool_base = pool_off[it.x];
+  const int e_max = (m.t0 + m.rows) / kpool;  // eligible pools of the item's last row
+  m.n_tiles = (e_max + kTilePools - 1) / kTilePools;
+  return m;
+}
+
+// Descending bitonic sort of n (a power of two) keys in shared memory, one warp.
+__device__ void warp_sort_desc(uint64_t* buf, int n) {
+  const int lane = threadIdx.x & 31;
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = lane; i < n; i += 32) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint64_t a = buf[i], b = buf[l];
+          const bool desc = (i & k) == 0;
+          if (desc ? (a < b) : (a > b)) {
+            buf[i] = b;
+            buf[l] = a;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+template <bool kNegScale>
+__global__ void __launch_bounds__(kThreads, 1)
+    select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
+                     const float* __restrict__ w, const int32_t* __restrict__ cu,
+                     const int32_t* __restrict__ pool_off, const int2* __restrict__ items,
+                     WorkspaceHeader* __restrict__ hdr, int kpool, int budget, float abs_scale,
+                     int32_t* __restrict__ out_ids, float* __restrict__ out_scores) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Bars bar = bars_at(smem);
+  int32_t* s_count = reinterpret_cast<int32_t*>(smem + kOffCount);
+  uint64_t* s_tau = reinterpret_cast<uint64_t*>(smem + kOffTau);
+  int32_t* s_elig = reinterpret_cast<int32_t*>(smem + kOffElig);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  int32_t* s_abort = reinterpret_cast<int32_t*>(smem + kOffMisc + 4);
+  float* s_w = reinterpret_cast<float*>(smem + kOffW);
+  uint64_t* s_cand = reinterpret_cast<uint64_t*>(smem + kOffCand);
+
+  // n_items was written by the planning kernel before this launch and is 0 when
+  // planning failed, so every thread reads the same value and the loops below
+  // agree on how many items there are.
+  const int n_items = hdr->n_items;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar.q_full, 1);
+    ptx::mbar_init(bar.q_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar.full + s, 1);
+      ptx::mbar_init(bar.empty + s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(bar.acc_full + a, 1);
+      ptx::mbar_init(bar.acc_empty + a, 8);
+    }
+    ptx::mbar_init(bar.mma_done, 1);
+    ptx::fence_mbar_init();
+    *s_abort = 0;
+    ptx::prefetch_tmap(&tmap_q);
+    ptx::prefetch_tmap(&tmap_kp);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(s_tmem, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  volatile int32_t* abort_flag = s_abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kp = ptx::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, q_phase = 0;
+      uint32_t fills = 0;  // pool-tile fills armed so far (stage = fill index mod kStages)
+      uint32_t q_armed = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_index(r, blockIdx.x, gridDim.x);
+        if (idx >= n_items) break;
+        const Item it = load_item(items, cu, pool_off, idx, kpool);
+        if (it.n_tiles == 0) continue;
+        if (!ptx::mbar_wait_bounded(bar.q_empty, q_phase ^ 1, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        q_phase ^= 1;
+        uint8_t* qdst = smem + kOffQ;
+        const int32_t qrow = int32_t((it.seq_start + it.t0) * kHeads);
+        ptx::mbar_arrive_expect_tx(bar.q_full, kQBytes);
+        ptx::tma_load_2d_hint(qdst, &tmap_q, bar.q_full, 0, qrow, pol_q);
+        ptx::tma_load_2d_hint(qdst + kQHalfBytes, &tmap_q, bar.q_full, 64, qrow, pol_q);
+        ++q_armed;
+        for (int i = 0; i < it.n_tiles; ++i) {
+          if (!ptx::mbar_wait_bounded(bar.empty + stage, phase ^ 1, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + kOffPool + stage * kStageBytes;
+          const int32_t prow = it.pool_base + i * kTilePools;
+          ptx::mbar_arrive_expect_tx(bar.full + stage, kStageBytes);
+          ptx::tma_load_2d_hint(dst, &tmap_kp, bar.full + stage, 0, prow, pol_kp);
+          ptx::tma_load_2d_hint(dst + kPoolHalfBytes, &tmap_kp, bar.full + stage, 64, prow, pol_kp);
+          ++fills;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // drain: the last fill armed on each barrier must land before the CTA exits
+      for (uint32_t s = 0; s < kStages; ++s) {
+        const uint32_t armed = (fills + kStages - 1 - s) / kStages;  // fills that went to stage s
+        if (armed) ptx::mbar_wait_bounded(bar.full + s, (armed - 1) & 1, kMaxPolls, kMaxWaitNs);
+      }
+      if (q_armed) ptx::mbar_wait_bounded(bar.q_full, (q_armed - 1) & 1, kMaxPolls, kMaxWaitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTilePools, kN);
+      const uint32_t q_addr = ptx::smem_addr(smem + kOffQ);
+      const uint32_t pool_addr = ptx::smem_addr(smem + kOffPool);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0, q_phase = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_index(r, blockIdx.x, gridDim.x);
+        if (idx >= n_items) break;
+        const Item it = load_item(items, cu, pool_off, idx, kpool);
+        if (it.n_tiles == 0) continue;
+        if (!ptx::mbar_wait_bounded(bar.q_full, q_phase, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        q_phase ^= 1;
+        ptx::tc_fence_after();
+        for (int i = 0; i < it.n_tiles; ++i) {
+          if (!ptx::mbar_wait_bounded(bar.acc_empty + acc, acc_phase ^ 1, kMaxPolls, kMaxWaitNs) ||
+              !ptx::mbar_wait_bounded(bar.full + stage, phase, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
+          const uint32_t a_base = pool_addr + stage * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kDim / 16; ++kk) {
+            const uint32_t a_addr = a_base + (kk >> 2) * kPoolHalfBytes + (kk & 3) * 32;
+            const uint32_t b_addr = q_addr + (kk >> 2) * kQHalfBytes + (kk & 3) * 32;
+            ptx::tc_mma_f16(d_tmem, ptx::smem_desc_kmajor_sw128(a_addr), ptx::smem_desc_kmajor_sw128(b_addr), idesc,
+                            kk > 0 ? 1u : 0u);
+          }
+          ptx::tc_commit(bar.empty + stage);
+          ptx::tc_commit(bar.acc_full + acc);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        }
+        if (!ok) break;
+        ptx::tc_commit(bar.q_empty);
+      }
+      if (!ok) {
+        record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // every MMA issued above must complete before TMEM is released
+      ptx::tc_commit(bar.mma_done);
+      ptx::mbar_wait_bounded(bar.mma_done, 0, kMaxPolls, kMaxWaitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;          // 0..7
+    const int half = ew >> 2;         // which four query rows of the item
+    const int wq = ew & 3;            // this warp's query row within the half (for selection work)
+    const int lg = warp & 3;          // TMEM lane group this warp may read
+    const int tw = wq * 32 + lane;    // thread index within the group of four warps
+    const int bar_id = 1 + half;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const uint32_t lane_addr = tmem_base + (uint32_t(lg * 32) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int r = 0;; ++r) {
+      const int idx = item_index(r, blockIdx.x, gridDim.x);
+      if (idx >= n_items) break;
+      const Item it = load_item(items, cu, pool_off, idx, kpool);
+      // per-item state of this half's four rows
+      for (int e = tw; e < 4 * kHeads; e += 128) {
+        const int qq = e / kHeads, h = e % kHeads;
+        const int row = it.t0 + half * 4 + qq;
+        s_w[(half * 4 + qq) * kHeads + h] =
+            row < it.len ? w[(it.seq_start + row) * kHeads + h] * abs_scale : 0.0f;
+      }
+      if (tw < 4) {
+        const int q = half * 4 + tw;
+        const int row = it.t0 + q;
+        s_count[q] = 0;
+        s_tau[q] = 0;
+        s_elig[q] = row < it.len ? (row + 1) / kpool : 0;
+      }
+      named_bar(bar_id, 128);
+      bool aborted = false;
+      for (int i = 0; i < it.n_tiles; ++i) {
+        bool ready = true;
+        if (lane == 0) ready = ptx::mbar_wait_bounded(bar.acc_full + acc, acc_phase, kMaxPolls, kMaxWaitNs);
+        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+        if (!ready) {
+          record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+          *abort_flag = 1;
+        }
+        if (ready) {
+          ptx::tc_fence_after();
+          uint32_t v[4][32];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            ptx::tc_ld_32x32b_x32(lane_addr + uint32_t(acc * kAccCols + (half * 4 + qq) * kHeads), v[qq]);
+          ptx::tc_wait_ld();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar.acc_empty + acc);
+          const int p = i * kTilePools + lg * 32 + lane;  // sequence-local pool index of this thread
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const int q = half * 4 + qq;
+            const float4* wv = reinterpret_cast<const float4*>(s_w + q * kHeads);
+            float s = 0.0f;
+#pragma unroll
+            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+              const float4 ww = wv[h4];
+              const float x0 = __uint_as_float(v[qq][4 * h4 + 0]);
+              const float x1 = __uint_as_float(v[qq][4 * h4 + 1]);
+              const float x2 = __uint_as_float(v[qq][4 * h4 + 2]);
+              const float x3 = __uint_as_float(v[qq][4 * h4 + 3]);
+              s = fmaf(ww.x, fmaxf(kNegScale ? -x0 : x0, 0.0f), s);
+              s = fmaf(ww.y, fmaxf(kNegScale ? -x1 : x1, 0.0f), s);
+              s = fmaf(ww.z, fmaxf(kNegScale ? -x2 : x2, 0.0f), s);
+              s = fmaf(ww.w, fmaxf(kNegScale ? -x3 : x3, 0.0f), s);
+            }
+            const uint64_t key = p < s_elig[q] ? make_key(s, uint32_t(p)) : 0ull;
+            const bool pass = key > s_tau[q];
+            const unsigned m = __ballot_sync(0xffffffffu, pass);
+            if (m) {
+              const int leader = __ffs(m) - 1;
+              int base = 0;
+              if (lane == leader) base = atomicAdd(s_count + q, __popc(m));
+              base = __shfl_sync(0xffffffffu, base, leader);
+              if (pass) s_cand[q * kCap + base + __popc(m & lt_mask)] = key;
+            }
+          }
+        }
+        if (named_bar_or(bar_id, 128, !ready || *abort_flag != 0)) {
+          aborted = true;
+          break;
+        }
+        {  // keep the candidate buffer of this warp's row below the compaction mark
+          const int q = half * 4 + wq;
+          const int n = s_count[q];
+          if (n > kCompactAt) {
+            uint64_t* buf = s_cand + q * kCap;
+            for (int e = n + lane; e < kCap; e += 32) buf[e] = 0;
+            __syncwarp();
+            warp_sort_desc(buf, kCap);
+            if (lane == 0) {
+              s_count[q] = budget;
+              s_tau[q] = buf[budget - 1];
+            }
+          }
+        }
+        named_bar(bar_id, 128);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (aborted) break;
+      {  // final ranking of this warp's row
+        const int q = half * 4 + wq;
+        const int row = it.t0 + q;
+        if (row < it.len) {
+          uint64_t* buf = s_cand + q * kCap;
+          const int n = s_count[q];
+          int width = 32;
+          while (width < n) width <<= 1;
+          for (int e = n + lane; e < width; e += 32) buf[e] = 0;
+          __syncwarp();
+          warp_sort_desc(buf, width);
+          const int64_t grow = it.seq_start + row;
+          for (int j = lane; j < budget; j += 32) {
+            const uint64_t key = j < width ? buf[j] : 0ull;
+            out_ids[grow * budget + j] = key ? int32_t(key_pool(key)) : -1;
+            if (out_scores) out_scores[grow * budget + j] = key ? key_score(key) : -INFINITY;
+          }
+        }
+      }
+      named_bar(bar_id, 128);
+    }
+    ptx::tc_fence_before();
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncwarp();
+  named_bar(3, kThreads);
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a [rows, 128] row-major matrix, box = 64 columns x box_rows,
+// 128-byte swizzle (the layout the MMA descriptors above expect).
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(kDim) * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool g_attr_set[64][2] = {};
+
+}  // namespace
+
+bool select_tc_supported(kpool_dtype dtype, int32_t H, int32_t d, int32_t budget) {
+  return dtype == KPOOL_BF16 && H == kHeads && d == kDim && budget >= 1 && budget <= kMaxBudget;
+}
+
+cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, const int32_t* cu, int32_t S, int64_t T,
+                             int32_t kpool, int32_t budget, float scale, int32_t* out_ids, float* out_scores,
+                             char* ws, const WorkspaceLayout& L, int grid, cudaStream_t stream) {
+  (void)S;
+  if (T == 0) return cudaSuccess;
+  if (T * kHeads > int64_t(INT32_MAX)) return cudaErrorInvalidValue;
+  CUtensorMap map_q, map_kp;
+  if (!make_map(&map_q, q, uint64_t(T) * kHeads, kN)) return cudaErrorInvalidValue;
+  const uint64_t kp_rows = L.max_pools > 0 ? uint64_t(L.max_pools) : 1;
+  if (!make_map(&map_kp, kp, kp_rows, kTilePools)) return cudaErrorInvalidValue;
+  const bool neg = scale < 0.0f;
+  const float abs_scale = neg ? -scale : scale;
+  auto kern = neg ? select_tc_kernel<true> : select_tc_kernel<false>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !g_attr_set[dev][neg ? 1 : 0]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) g_attr_set[dev][neg ? 1 : 0] = true;
+  }
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(
+      map_q, map_kp, w, cu, reinterpret_cast<const int32_t*>(ws + L.pool_off),
+      reinterpret_cast<const int2*>(ws + L.items), reinterpret_cast<WorkspaceHeader*>(ws + L.header), kpool, budget,
+      abs_scale, out_ids, out_scores);
+  return cudaGetLastError();
+}
+
+}  // namespace kpool

@@ -1,0 +1,211 @@
+"""ctypes binding of the CUDA library (C ABI in include/kpool.h).
+
+Argument marshalling only: every step of the selection runs in the library's
+kernels. Functions carry the C names. Tensors must be CUDA tensors on the
+current device; outputs and workspace are allocated with torch when the caller
+does not pass them (the library itself never allocates). Calls run on torch's
+current CUDA stream unless `stream` is given.
+
+There is no fallback: if the library is not built, or a call fails, these
+functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkpool.so")
+
+KPOOL_OK = 0
+KPOOL_ERR_INVALID_ARG = 1
+KPOOL_ERR_UNSUPPORTED = 2
+KPOOL_ERR_WORKSPACE = 3
+KPOOL_ERR_CUDA = 4
+KPOOL_ERR_DEVICE_TIMEOUT = 5
+
+KPOOL_BF16 = 0
+KPOOL_F32 = 1
+
+KPOOL_SCORE_AUTO = 0
+KPOOL_SCORE_TC = 1
+KPOOL_SCORE_SIMT = 2
+
+EXPORTED = (
+    "kpool_workspace_bytes", "kpool_select", "kpool_select_ex", "kpool_pool_keys", "kpool_expand",
+    "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string",
+)
+
+
+class KpoolError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {kpool_status_string(status)} (status {status})")
+
+
+class kpool_options(ctypes.Structure):
+    _fields_ = [("score_kernel", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 6)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Open the built library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"the KPool CUDA library is not built ({LIB_PATH} missing); "
+                               "run `python -m sparse_attention_kpool_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        lib.kpool_workspace_bytes.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+        lib.kpool_workspace_bytes.restype = sz
+        sel = [P, P, P, P, i32, i64, i32, i32, i32, i32, i32, f32, P, P, P, P, sz, P]
+        lib.kpool_select.argtypes = sel
+        lib.kpool_select.restype = i32
+        lib.kpool_select_ex.argtypes = sel + [ctypes.POINTER(kpool_options)]
+        lib.kpool_select_ex.restype = i32
+        lib.kpool_pool_keys.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, sz, P]
+        lib.kpool_pool_keys.restype = i32
+        lib.kpool_expand.argtypes = [P, P, i32, i64, i32, i32, P, P]
+        lib.kpool_expand.restype = i32
+        lib.kpool_last_device_error.argtypes = [P, P]
+        lib.kpool_last_device_error.restype = i32
+        lib.kpool_wait_timeout_selftest.argtypes = [P, sz, i64, P]
+        lib.kpool_wait_timeout_selftest.restype = i32
+        lib.kpool_status_string.argtypes = [i32]
+        lib.kpool_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def kpool_status_string(status: int) -> str:
+    return load().kpool_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KPOOL_BF16
+    if t.dtype == torch.float32:
+        return KPOOL_F32
+    raise TypeError(f"q/k must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def kpool_workspace_bytes(total_tokens: int, num_seqs: int, heads: int, head_dim: int, dtype: int, kpool: int,
+                          index_topk: int) -> int:
+    return int(load().kpool_workspace_bytes(total_tokens, num_seqs, heads, head_dim, dtype, kpool, index_topk))
+
+
+def new_workspace(total_tokens: int, num_seqs: int, heads: int, head_dim: int, dtype: int, kpool: int,
+                  index_topk: int, device=None) -> torch.Tensor:
+    n = kpool_workspace_bytes(total_tokens, num_seqs, heads, head_dim, dtype, kpool, index_topk)
+    if n == 0:
+        raise KpoolError(KPOOL_ERR_INVALID_ARG, "kpool_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def kpool_select_ex(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor, kpool: int,
+                    index_topk: int, scale: float, out_pool_ids=None, out_token_ids=None, out_pool_scores=None,
+                    return_scores: bool = False, workspace=None, stream=None, score_kernel: int = KPOOL_SCORE_AUTO,
+                    max_ctas: int = 0):
+    """q [T,H,d], k [T,d] (bf16 or fp32), w [T,H] fp32, cu_seqlens [S+1] int32 -> (pool_ids [T,B],
+    token_ids [T, index_topk+kpool], pool_scores [T,B] or None)."""
+    T, H, d = q.shape
+    S = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or w.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("k must match q's dtype; w must be float32; cu_seqlens int32")
+    B = index_topk // kpool if kpool > 0 else 0
+    dev = q.device
+    if out_pool_ids is None:
+        out_pool_ids = torch.empty((T, B), dtype=torch.int32, device=dev)
+    if out_token_ids is None:
+        out_token_ids = torch.empty((T, index_topk + kpool), dtype=torch.int32, device=dev)
+    if out_pool_scores is None and return_scores:
+        out_pool_scores = torch.empty((T, B), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(T, S, H, d, dt, kpool, index_topk, dev)
+    _check_cuda(q, k, w, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores, workspace)
+    opts = kpool_options(score_kernel, max_ctas)
+    st = load().kpool_select_ex(_ptr(q), _ptr(k), _ptr(w), _ptr(cu_seqlens), S, T, H, d, dt, kpool, index_topk,
+                                float(scale), _ptr(out_pool_ids), _ptr(out_token_ids), _ptr(out_pool_scores),
+                                _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_select")
+    return out_pool_ids, out_token_ids, out_pool_scores
+
+
+def kpool_select(q, k, w, cu_seqlens, kpool, index_topk, scale, out_pool_ids=None, out_token_ids=None,
+                 out_pool_scores=None, return_scores=False, workspace=None, stream=None):
+    """The whole selection with default options (see kpool_select_ex)."""
+    return kpool_select_ex(q, k, w, cu_seqlens, kpool, index_topk, scale, out_pool_ids, out_token_ids,
+                           out_pool_scores, return_scores, workspace, stream)
+
+
+def kpool_pool_keys(k: torch.Tensor, cu_seqlens: torch.Tensor, kpool: int, out=None, workspace=None, stream=None):
+    """Mean-pooled keys; returns a [T // kpool, d] tensor whose first P rows are the pools."""
+    T, d = k.shape
+    S = cu_seqlens.numel() - 1
+    dt = _dtype_code(k)
+    if out is None:
+        out = torch.empty((max(T // kpool, 0), d), dtype=k.dtype, device=k.device)
+    if workspace is None:
+        workspace = new_workspace(T, S, 1, d, dt, kpool, 0, k.device)
+    _check_cuda(k, cu_seqlens, out, workspace)
+    st = load().kpool_pool_keys(_ptr(k), _ptr(cu_seqlens), S, T, d, dt, kpool, _ptr(out), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_pool_keys")
+    return out
+
+
+def kpool_expand(pool_ids: torch.Tensor, cu_seqlens: torch.Tensor, kpool: int, index_topk: int, out=None,
+                 stream=None):
+    T = pool_ids.shape[0]
+    S = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((T, index_topk + kpool), dtype=torch.int32, device=pool_ids.device)
+    _check_cuda(pool_ids, cu_seqlens, out)
+    st = load().kpool_expand(_ptr(pool_ids), _ptr(cu_seqlens), S, T, kpool, index_topk, _ptr(out), _stream(stream))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_expand")
+    return out
+
+
+def kpool_last_device_error(workspace: torch.Tensor, stream=None) -> int:
+    return int(load().kpool_last_device_error(_ptr(workspace), _stream(stream)))
+
+
+def kpool_wait_timeout_selftest(workspace: torch.Tensor, spin_limit: int, stream=None) -> int:
+    return int(load().kpool_wait_timeout_selftest(_ptr(workspace), workspace.numel(), int(spin_limit),
+                                                  _stream(stream)))

@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads,
+exports every entry point include/kpool.h declares, sizes workspaces, and rejects
+bad arguments before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from sparse_attention_kpool_gb300 import build as kbuild
+from sparse_attention_kpool_gb300 import kpool as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kpool.h")
+
+# Fake, 256-byte aligned, never dereferenced addresses: every call below fails
+# validation before any pointer is used.
+FAKE = 0x7F0000000000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return K.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kpool_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(K.EXPORTED)
+
+
+def test_library_exports_every_declared_function(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", K.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_functions():
+        assert name in exported, f"{name} declared in kpool.h but not exported"
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert K.kpool_status_string(st)
+    assert K.kpool_status_string(99) == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    a = K.kpool_workspace_bytes(8192, 2, 32, 128, K.KPOOL_BF16, 4, 2048)
+    b = K.kpool_workspace_bytes(16384, 2, 32, 128, K.KPOOL_BF16, 4, 2048)
+    assert a > 0 and b > a and a % 256 == 0
+    # the pooled keys dominate: P * d * 2 bytes
+    assert a >= 2048 * 128 * 2
+    assert K.kpool_workspace_bytes(8192, 2, 32, 128, K.KPOOL_BF16, 3, 2048) == 0   # index_topk % kpool
+    assert K.kpool_workspace_bytes(8192, 2, 32, 128, K.KPOOL_BF16, 0, 2048) == 0   # kpool < 1
+    assert K.kpool_workspace_bytes(8192, 0, 32, 128, K.KPOOL_BF16, 4, 2048) == 0   # no sequences
+    assert K.kpool_workspace_bytes(8192, 1, 32, 100, K.KPOOL_BF16, 4, 2048) == 0   # rows not 16-byte multiples
+    assert K.kpool_workspace_bytes(-1, 1, 32, 128, K.KPOOL_BF16, 4, 2048) == 0
+    assert K.kpool_workspace_bytes(0, 0, 32, 128, K.KPOOL_BF16, 4, 2048) > 0      # empty batch is valid
+
+
+def _select(lib, T=64, S=1, H=4, d=32, dtype=K.KPOOL_F32, kpool=4, topk=16, scale=0.5, q=FAKE, k=FAKE, w=FAKE,
+            cu=FAKE, ids=FAKE, toks=FAKE, scores=None, ws=FAKE, ws_bytes=1 << 30, opts=None):
+    P = ctypes.c_void_p
+    return lib.kpool_select_ex(P(q), P(k), P(w), P(cu), S, T, H, d, dtype, kpool, topk, scale, P(ids), P(toks),
+                               P(scores) if scores else None, P(ws), ws_bytes, None,
+                               ctypes.byref(opts) if opts else None)
+
+
+def test_select_rejects_bad_arguments(lib):
+    assert _select(lib, kpool=0) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, kpool=3, topk=16) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, topk=-4) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, H=0) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, d=30) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, dtype=7) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, S=0) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, T=-5) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, scale=float("nan")) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, scale=float("inf")) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, q=0) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, toks=0) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, ids=0) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, q=FAKE + 8) == K.KPOOL_ERR_INVALID_ARG      # q must be 16-byte aligned
+    assert _select(lib, k=FAKE + 4) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, ws=0) == K.KPOOL_ERR_WORKSPACE
+    assert _select(lib, ws=FAKE + 64) == K.KPOOL_ERR_WORKSPACE     # 256-byte alignment
+    assert _select(lib, ws_bytes=1024) == K.KPOOL_ERR_WORKSPACE
+    bad = K.kpool_options(K.KPOOL_SCORE_AUTO, 0)
+    bad.reserved[2] = 1
+    assert _select(lib, opts=bad) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, opts=K.kpool_options(9, 0)) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, opts=K.kpool_options(0, -1)) == K.KPOOL_ERR_INVALID_ARG
+
+
+def test_select_rejects_unsupported_kernel_choice(lib):
+    # the tensor-core kernel needs bf16, H = 32, d = 128, budget <= 512
+    tc = K.kpool_options(K.KPOOL_SCORE_TC, 0)
+    assert _select(lib, opts=tc) == K.KPOOL_ERR_UNSUPPORTED                       # fp32, H 4, d 32
+    assert _select(lib, H=32, d=128, dtype=K.KPOOL_BF16, topk=4096, opts=tc) == K.KPOOL_ERR_UNSUPPORTED
+    assert _select(lib, H=65, d=128, dtype=K.KPOOL_BF16) == K.KPOOL_ERR_UNSUPPORTED
+    assert _select(lib, H=4, d=512, dtype=K.KPOOL_BF16) == K.KPOOL_ERR_UNSUPPORTED
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert _select(lib, T=0, S=0, q=0, k=0, w=0, cu=0, ids=0, toks=0, ws=0) == K.KPOOL_OK
+
+
+def test_pool_keys_and_expand_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.kpool_pool_keys(P(FAKE), P(FAKE), 1, 64, 32, K.KPOOL_F32, 0, P(FAKE), P(FAKE), 1 << 20,
+                               None) == K.KPOOL_ERR_INVALID_ARG
+    assert lib.kpool_pool_keys(P(FAKE), P(FAKE), 1, 64, 32, K.KPOOL_F32, 4, P(FAKE), P(FAKE), 16,
+                               None) == K.KPOOL_ERR_WORKSPACE
+    assert lib.kpool_pool_keys(P(FAKE + 4), P(FAKE), 1, 64, 32, K.KPOOL_F32, 4, P(FAKE), P(FAKE), 1 << 20,
+                               None) == K.KPOOL_ERR_INVALID_ARG
+    assert lib.kpool_expand(P(FAKE), P(FAKE), 1, 64, 4, 6, P(FAKE), None) == K.KPOOL_ERR_INVALID_ARG
+    assert lib.kpool_expand(None, P(FAKE), 1, 64, 4, 16, P(FAKE), None) == K.KPOOL_ERR_INVALID_ARG
+    assert lib.kpool_expand(None, None, 0, 0, 4, 16, None, None) == K.KPOOL_OK
+
+
+def test_selftest_and_error_query_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.kpool_wait_timeout_selftest(None, 1 << 20, 10, None) == K.KPOOL_ERR_WORKSPACE
+    assert lib.kpool_wait_timeout_selftest(P(FAKE), 64, 10, None) == K.KPOOL_ERR_WORKSPACE
+    assert lib.kpool_wait_timeout_selftest(P(FAKE), 1 << 20, 0, None) == K.KPOOL_ERR_INVALID_ARG
+    assert lib.kpool_last_device_error(None, None) == K.KPOOL_ERR_WORKSPACE
+    assert lib.kpool_last_device_error(P(FAKE + 8), None) == K.KPOOL_ERR_WORKSPACE
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(K, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(K, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        K.load()

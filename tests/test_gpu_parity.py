@@ -1,0 +1,311 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Integer-valued inputs must match bit for bit (ids, order, tokens); float inputs
+follow the tolerance rule in tests/parity.py. Small cases compare every row;
+the full-size workloads compare a stratified row sample plus properties that
+hold at any size on every row.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from sparse_attention_kpool_gb300 import build as kbuild
+from sparse_attention_kpool_gb300 import kpool as K
+from sparse_attention_kpool_gb300 import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+TC, SIMT = K.KPOOL_SCORE_TC, K.KPOOL_SCORE_SIMT
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    kbuild.build()
+    K.load()
+    oracle.build()
+
+
+def to_dev(inp):
+    return {k: v.cuda() for k, v in inp.items()}
+
+
+def run(dev, wl, **kw):
+    ids, toks, sc = K.kpool_select_ex(dev["q"], dev["k"], dev["w"], dev["cu_seqlens"], wl.kpool, wl.index_topk,
+                                      wl.scale, return_scores=True, **kw)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), toks.cpu().numpy(), sc.cpu().numpy()
+
+
+def full_oracle(inp, wl):
+    return parity.oracle_rows(inp, wl, np.arange(wl.total_tokens))
+
+
+def check_properties(dev, wl, ids, scores, toks):
+    """Properties every row must satisfy, checked on the GPU for all rows."""
+    cu = dev["cu_seqlens"].long()
+    T, B, kp = wl.total_tokens, wl.budget, wl.kpool
+    rows = torch.arange(T, device="cuda")
+    seq = torch.searchsorted(cu[1:], rows, right=True)
+    t = rows - cu[seq]
+    L = cu[seq + 1] - cu[seq]
+    e = (t + 1) // kp
+    ids = torch.as_tensor(ids, device="cuda").long()
+    sc = torch.as_tensor(scores, device="cuda")
+    m = torch.clamp(e, max=B)
+    slot = torch.arange(B, device="cuda")[None, :]
+    valid = slot < m[:, None]
+    assert bool(((ids >= 0) == valid).all()), "padding / count"
+    assert bool((ids[valid] < e[:, None].expand_as(ids)[valid]).all()), "pool beyond the row"
+    srt = torch.sort(torch.where(valid, ids, torch.full_like(ids, 1 << 40)), dim=1).values
+    d = srt[:, 1:] - srt[:, :-1]
+    assert bool(((d > 0) | ~valid[:, 1:]).all()), "duplicate pools"
+    both = valid[:, 1:]
+    assert bool(((sc[:, :-1] >= sc[:, 1:]) | ~both).all()), "scores not ranked"
+    tie = (sc[:, :-1] == sc[:, 1:]) & both
+    assert bool(((ids[:, :-1] < ids[:, 1:]) | ~tie).all()), "tie not broken toward the smaller pool"
+    # tokens: expansion of the ids, then the tail, nothing beyond the row
+    tok = torch.as_tensor(toks, device="cuda").long()
+    r = torch.arange(kp, device="cuda")
+    want = torch.where(ids[:, :, None] >= 0, ids[:, :, None] * kp + r, torch.full_like(ids[:, :, None], -1))
+    assert bool((tok[:, :B * kp].reshape(T, B, kp) == want).all()), "expansion"
+    tail_len = (t + 1) % kp
+    want_tail = torch.where(r[None, :] < tail_len[:, None], e[:, None] * kp + r, torch.full_like(e[:, None], -1))
+    assert bool((tok[:, B * kp:] == want_tail).all()), "tail"
+    assert bool(((tok <= t[:, None]) & (tok < L[:, None]) | (tok == -1)).all()), "mask"
+
+
+# ------------------------------------------------------------------ pooling
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_pool_keys_bit_exact(dtype):
+    wl = W.custom("pool", (5, 0, 130, 1027, 3), heads=1, head_dim=128 if dtype == "bf16" else 32, kpool=4,
+                  index_topk=4, scale=1.0, dtype=dtype, values="normal", seed=41)
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    kp = K.kpool_pool_keys(dev["k"], dev["cu_seqlens"], wl.kpool)
+    torch.cuda.synchronize()
+    ref = oracle.pool(parity.bits(inp["k"]), dtype, inp["cu_seqlens"].numpy(), wl.kpool)
+    got = kp[: ref.shape[0]].float().cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("kpool", [3, 5])
+def test_pool_keys_odd_kpool(kpool):
+    wl = W.custom("poolk", (64, 21), heads=1, head_dim=64, kpool=kpool, index_topk=kpool, scale=1.0,
+                  dtype="bf16", values="normal", seed=42)
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    kp = K.kpool_pool_keys(dev["k"], dev["cu_seqlens"], kpool)
+    torch.cuda.synchronize()
+    ref = oracle.pool(parity.bits(inp["k"]), "bf16", inp["cu_seqlens"].numpy(), kpool)
+    np.testing.assert_array_equal(kp[: ref.shape[0]].float().cpu().numpy(), ref)
+
+
+# ------------------------------------------------------- selection: exact
+
+@pytest.mark.parametrize("kernel", [TC, SIMT])
+def test_integer_ragged_exact(kernel):
+    """Integer-valued inputs: every score is exact in fp32, so ids, order and tokens match bit for bit.
+    Sequences span several pool tiles, a ragged last item and rows long enough to compact."""
+    wl = W.custom("int", (1, 3, 517, 0, 4100, 64, 2053, 9), heads=32, head_dim=128, kpool=4, index_topk=2048,
+                  scale=1.0 / 16, dtype="bf16", values="integer", seed=43, dup_every=8)
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    ids, toks, sc = run(dev, wl, score_kernel=kernel)
+    ref = full_oracle(inp, wl)
+    parity.assert_exact(ref, ids, toks)
+    m = ref["pool_ids"] >= 0
+    np.testing.assert_array_equal(sc[m], ref["scores"][m].astype(np.float32))
+    check_properties(dev, wl, ids, sc, toks)
+
+
+def test_tie_heavy_workload_exact():
+    """The tie-heavy workload (2 x 4096, integer-valued, duplicated pools): every row bit-exact."""
+    wl = W.TIE_HEAVY
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    ids, toks, sc = run(dev, wl)
+    ref = full_oracle(inp, wl)
+    parity.assert_exact(ref, ids, toks)
+    check_properties(dev, wl, ids, sc, toks)
+    # the recipe does produce exact ties at the cutoff
+    kp = ref["kp"]
+    assert (ref["eligible"] > wl.budget).any()
+
+
+@pytest.mark.parametrize("kernel", [TC, SIMT])
+def test_edge_cases_exact(kernel):
+    cases = [
+        W.custom("kpool1", (300, 2), 32, 128, 1, 64, 1.0 / 16, "bf16", "integer", 51),
+        W.custom("kpool3", (301, 7, 2), 32, 128, 3, 48, 1.0 / 16, "bf16", "integer", 52, dup_every=5),
+        W.custom("negscale", (400,), 32, 128, 4, 64, -1.0 / 16, "bf16", "integer", 53),
+        W.custom("zeroscale", (200,), 32, 128, 4, 32, 0.0, "bf16", "integer", 54),
+        W.custom("short", (1, 2, 3, 0, 5), 32, 128, 4, 16, 1.0 / 16, "bf16", "integer", 55),
+        W.custom("allpools", (130,), 32, 128, 4, 2048, 1.0 / 16, "bf16", "integer", 56),
+        W.custom("onebudget", (260,), 32, 128, 4, 4, 1.0 / 16, "bf16", "integer", 57, dup_every=2),
+    ]
+    for wl in cases:
+        inp = W.generate(wl, "cpu")
+        dev = to_dev(inp)
+        ids, toks, sc = run(dev, wl, score_kernel=kernel)
+        ref = full_oracle(inp, wl)
+        parity.assert_exact(ref, ids, toks)
+        check_properties(dev, wl, ids, sc, toks)
+
+
+def test_negative_weights_exact():
+    wl = W.custom("negw", (700,), 32, 128, 4, 128, 1.0 / 16, "bf16", "integer", 58)
+    inp = W.generate(wl, "cpu")
+    inp["w"] = inp["w"] - 0.5   # multiples of 1/4 in [-0.5, 0.5]: still exact
+    dev = to_dev(inp)
+    for kernel in (TC, SIMT):
+        ids, toks, sc = run(dev, wl, score_kernel=kernel)
+        parity.assert_exact(full_oracle(inp, wl), ids, toks)
+
+
+def test_results_independent_of_grid_and_kernel():
+    wl = W.custom("grid", (3000, 1111), 32, 128, 4, 2048, 1.0 / 16, "bf16", "integer", 59, dup_every=8)
+    dev = to_dev(W.generate(wl, "cpu"))
+    base = run(dev, wl, score_kernel=TC)
+    for kw in ({"score_kernel": TC, "max_ctas": 1}, {"score_kernel": TC, "max_ctas": 7},
+               {"score_kernel": SIMT}, {"score_kernel": SIMT, "max_ctas": 3}):
+        got = run(dev, wl, **kw)
+        for a, b in zip(base, got):
+            np.testing.assert_array_equal(a, b, err_msg=str(kw))
+
+
+def test_packed_equals_alone_gpu():
+    wl = W.custom("pack", (999, 2500, 17), 32, 128, 4, 2048, 1.0 / 16, "bf16", "integer", 60, dup_every=8)
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    ids, toks, _ = run(dev, wl)
+    cu = inp["cu_seqlens"].tolist()
+    for b in range(wl.num_seqs):
+        s, e = cu[b], cu[b + 1]
+        one = W.custom("one", (e - s,), 32, 128, 4, 2048, 1.0 / 16, "bf16", "integer", 0)
+        d1 = {"q": dev["q"][s:e].contiguous(), "k": dev["k"][s:e].contiguous(), "w": dev["w"][s:e].contiguous(),
+              "cu_seqlens": torch.tensor([0, e - s], dtype=torch.int32, device="cuda")}
+        i1, t1, _ = run(d1, one)
+        np.testing.assert_array_equal(ids[s:e], i1)
+        np.testing.assert_array_equal(toks[s:e], t1)
+
+
+def test_head_permutation_gpu():
+    wl = W.custom("perm", (1500,), 32, 128, 4, 1024, 1.0 / 16, "bf16", "integer", 61)
+    dev = to_dev(W.generate(wl, "cpu"))
+    base = run(dev, wl)
+    perm = torch.randperm(32, generator=torch.Generator().manual_seed(3)).cuda()
+    dev2 = dict(dev, q=dev["q"][:, perm].contiguous(), w=dev["w"][:, perm].contiguous())
+    got = run(dev2, wl)
+    np.testing.assert_array_equal(base[0], got[0])
+    np.testing.assert_array_equal(base[2], got[2])
+
+
+# ------------------------------------------------------- selection: float
+
+def test_tiny_workload_f32():
+    wl = W.TINY
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    ids, toks, sc = run(dev, wl)
+    ref = full_oracle(inp, wl)
+    parity.compare_float(inp, wl, ref, ids, sc, toks)
+    check_properties(dev, wl, ids, sc, toks)
+
+
+def test_float_small_all_rows():
+    wl = W.custom("flt", (3000, 700, 5), 32, 128, 4, 2048, 1.0 / np.sqrt(128), "bf16", "normal", 62)
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    ids, toks, sc = run(dev, wl)
+    ref = full_oracle(inp, wl)
+    stats = parity.compare_float(inp, wl, ref, ids, sc, toks)
+    check_properties(dev, wl, ids, sc, toks)
+    assert stats["near_tie_rows"] <= 0.05 * wl.total_tokens
+
+
+def _sampled(wl, count):
+    dev = W.generate(wl, "cuda")
+    ids, toks, sc = K.kpool_select_ex(dev["q"], dev["k"], dev["w"], dev["cu_seqlens"], wl.kpool, wl.index_topk,
+                                      wl.scale, return_scores=True)
+    torch.cuda.synchronize()
+    check_properties(dev, wl, ids, sc, toks)
+    rows = W.sample_rows(wl, count).numpy()
+    ref = parity.oracle_rows(dev, wl, rows)
+    r = torch.as_tensor(rows, device="cuda")
+    stats = parity.compare_float(dev, wl, ref, ids[r].cpu().numpy(), sc[r].cpu().numpy(), toks[r].cpu().numpy())
+    return stats
+
+
+def test_varlen_workload_sampled():
+    stats = _sampled(W.VARLEN, 1500)
+    assert stats["near_tie_rows"] <= 0.05 * stats["rows"]
+
+
+def test_long_128k_workload_sampled():
+    stats = _sampled(W.LONG_128K, 300)
+    assert stats["near_tie_rows"] <= 0.05 * stats["rows"]
+
+
+def test_pages_512k_workload_sampled():
+    stats = _sampled(W.PAGES_512K, 96)
+    assert stats["near_tie_rows"] <= 0.1 * stats["rows"]
+
+
+def test_repeat_calls_identical():
+    wl = W.custom("rep", (5000,), 32, 128, 4, 2048, 1.0 / np.sqrt(128), "bf16", "normal", 63)
+    dev = to_dev(W.generate(wl, "cpu"))
+    a = run(dev, wl)
+    b = run(dev, wl)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+# ------------------------------------------------------- errors and guards
+
+def test_outputs_stay_inside_their_buffers():
+    wl = W.custom("canary", (777, 130), 32, 128, 4, 256, 1.0 / 16, "bf16", "integer", 64)
+    dev = to_dev(W.generate(wl, "cpu"))
+    T, B, Wd = wl.total_tokens, wl.budget, wl.width
+    pad = 4096
+    ids_buf = torch.full((T * B + 2 * pad,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    tok_buf = torch.full((T * Wd + 2 * pad,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    sc_buf = torch.full((T * B + 2 * pad,), 1234.5, dtype=torch.float32, device="cuda")
+    ids = ids_buf[pad:pad + T * B].view(T, B)
+    toks = tok_buf[pad:pad + T * Wd].view(T, Wd)
+    sc = sc_buf[pad:pad + T * B].view(T, B)
+    K.kpool_select_ex(dev["q"], dev["k"], dev["w"], dev["cu_seqlens"], wl.kpool, wl.index_topk, wl.scale,
+                      out_pool_ids=ids, out_token_ids=toks, out_pool_scores=sc)
+    torch.cuda.synchronize()
+    for buf, val in ((ids_buf, 0x5A5A5A5A), (tok_buf, 0x5A5A5A5A)):
+        assert bool((buf[:pad] == val).all()) and bool((buf[-pad:] == val).all())
+    assert bool((sc_buf[:pad] == 1234.5).all()) and bool((sc_buf[-pad:] == 1234.5).all())
+    assert bool((ids >= -1).all()) and not bool((toks == 0x5A5A5A5A).any())
+
+
+def test_malformed_cu_seqlens_reported_on_device():
+    wl = W.custom("badcu", (64, 64), 32, 128, 4, 64, 1.0, "bf16", "integer", 65)
+    dev = to_dev(W.generate(wl, "cpu"))
+    ws = K.new_workspace(128, 2, 32, 128, K.KPOOL_BF16, 4, 64)
+    for bad in ([0, 100, 90], [1, 64, 128], [0, 64, 127]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        toks = torch.full((128, 68), 777, dtype=torch.int32, device="cuda")
+        K.kpool_select_ex(dev["q"], dev["k"], dev["w"], cu, 4, 64, 1.0, out_token_ids=toks, workspace=ws)
+        assert K.kpool_last_device_error(ws) == K.KPOOL_ERR_INVALID_ARG
+        assert bool((toks == 777).all()), "nothing may be written when the bounds are malformed"
+    # a well-formed call on the same workspace clears the error
+    K.kpool_select_ex(dev["q"], dev["k"], dev["w"], dev["cu_seqlens"], 4, 64, 1.0, workspace=ws)
+    assert K.kpool_last_device_error(ws) == K.KPOOL_OK
+
+
+def test_bounded_wait_reports_timeout_without_hanging():
+    ws = K.new_workspace(64, 1, 32, 128, K.KPOOL_BF16, 4, 16)
+    assert K.kpool_wait_timeout_selftest(ws, 1000) == K.KPOOL_OK
+    assert K.kpool_last_device_error(ws) == K.KPOOL_ERR_DEVICE_TIMEOUT
+    # the context is still usable afterwards
+    wl = W.custom("after", (100,), 32, 128, 4, 16, 1.0 / 16, "bf16", "integer", 66)
+    inp = W.generate(wl, "cpu")
+    ids, toks, _ = run(to_dev(inp), wl)
+    parity.assert_exact(full_oracle(inp, wl), ids, toks)
