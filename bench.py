@@ -1,0 +1,419 @@
+"""Benchmark of the KPool indexer selection on synthetic GLM-shaped inputs.
+
+One step = one kpool_select call (plan, pool, score+select, expand) over the
+whole batch. Default workload: the pages-scale causal batch, 1 x 524288 tokens,
+32 index heads, d = 128, kpool 4, index_topk 2048 (budget 512 pools), bf16 q/k,
+fp32 head weights -- the configuration the pages quote their selection time on.
+
+Prints one JSON line (rank 0). `value` is whole-job throughput in scored
+(query row, eligible pool) pairs per second with inputs resident in HBM;
+`e2e` is the same metric through the C ABI with host (pinned) buffers and the
+host<->device copies inside the timed region. `roofline` reports the
+score+select kernel against the measured bf16 tensor-core peak, timed with CUDA
+events that the library records around each of its kernels. `cpu_baseline` is
+the CPU oracle timed on a bounded row sample on this host's cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU: replicas only -- every rank runs its own copy of the workload (the
+selection has no exchange step on one node), barrier + max-over-ranks timing,
+value = all ranks' pairs / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_attention_kpool_gb300 import build as kbuild  # noqa: E402
+from sparse_attention_kpool_gb300 import kpool as K  # noqa: E402
+from sparse_attention_kpool_gb300 import workloads as W  # noqa: E402
+
+METRIC = "KPool selection sec @512k tokens; scored pairs/s; % of bf16 tensor-core peak"
+UNIT = "scored pairs/s"
+FLOP_PER_PAIR_PER_HEAD_DIM = 2  # one multiply-add per (head, channel) of a scored pair
+
+# DRAM traffic of the score+select kernel from one ncu capture, per launch at the
+# pages-scale workload, tied to the kernel source it was measured on: when the
+# source hash differs the number is stale and is reported as null.
+NCU_TRAFFIC = {"kernel_sha256": None, "workload": None, "bytes_per_launch": None}
+
+
+def source_sha(path: str) -> str:
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "_source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        self.device_index = device_index
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        bus = _pci_bus_id(self.device_index)
+        if bus:
+            cmd += ["-i", bus]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _pci_bus_id(dev: int):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        dom, bus, d = getattr(p, "pci_domain_id", None), getattr(p, "pci_bus_id", None), getattr(p, "pci_device_id", None)
+        if bus is None:
+            return None
+        return f"{dom or 0:08X}:{bus:02X}:{d or 0:02X}.0"
+    except Exception:
+        return None
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(dev_inputs: dict, wl: W.Workload, rows: np.ndarray, kp=None):
+    """Time the CPU oracle on the listed rows (the bounded CPU baseline sample)."""
+    from oracle import oracle
+    from tests import parity
+    cu = dev_inputs["cu_seqlens"].cpu().numpy()
+    k_bits = parity.bits(dev_inputs["k"])
+    ridx = torch.as_tensor(rows, device=dev_inputs["q"].device)
+    q_rows = parity.bits(dev_inputs["q"][ridx])
+    w_rows = dev_inputs["w"][ridx].cpu().numpy()
+    t0 = time.perf_counter()
+    if kp is None:
+        kp = oracle.pool(k_bits, wl.dtype, cu, wl.kpool)
+    out = oracle.select(q_rows, w_rows, kp, cu, rows, wl.dtype, wl.kpool, wl.index_topk, wl.scale)
+    dt = time.perf_counter() - t0
+    pairs = int(out["eligible"].sum())
+    return {"seconds": dt, "pairs": pairs, "threads": oracle.threads(), "out": out, "kp": kp}
+
+
+def pick_sample_rows(wl: W.Workload, target_pairs: float, seed: int) -> np.ndarray:
+    """Uniform rows until their eligible-pool count reaches target_pairs."""
+    rng = np.random.default_rng(seed)
+    T = wl.total_tokens
+    cu = wl.cu_seqlens().numpy()
+    rows, pairs = [], 0
+    while pairs < target_pairs and len(rows) < T:
+        r = int(rng.integers(0, T))
+        b = int(np.searchsorted(cu, r, side="right") - 1)
+        pairs += (r - int(cu[b]) + 1) // wl.kpool
+        rows.append(r)
+    return np.array(sorted(set(rows)), dtype=np.int64)
+
+
+def reference_arm(args, wl, world, rank):
+    """The oracle as the reference implementation: each step scores a bounded row sample."""
+    if rank != 0:
+        return
+    torch.manual_seed(0)
+    inp = W.generate(wl, "cpu" if not torch.cuda.is_available() else "cuda")
+    from oracle import oracle
+    oracle.build()
+    cu = inp["cu_seqlens"].cpu().numpy()
+    from tests import parity
+    kp = oracle.pool(parity.bits(inp["k"]), wl.dtype, cu, wl.kpool)
+    times, pairs_all = [], []
+    for step in range(args.warmup + args.steps):
+        rows = pick_sample_rows(wl, args.ref_pairs_per_step, seed=1000 + step)
+        res = oracle_sample(inp, wl, rows, kp=kp)
+        if step >= args.warmup:
+            times.append(res["seconds"])
+            pairs_all.append(res["pairs"])
+    total_t, total_p = sum(times), sum(pairs_all)
+    value = total_p / total_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "seqlens": list(wl.seqlens), "heads": wl.heads, "head_dim": wl.head_dim,
+                   "kpool": wl.kpool, "index_topk": wl.index_topk, "budget": wl.budget,
+                   "inputs": "q,k bf16 N(0,1), w fp32 U(0,1), seeded"},
+        "sec_per_selection_extrapolated": wl.causal_pairs() / value,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{len(times)} steps x ~{args.ref_pairs_per_step:.2e} pairs of uniform rows "
+                                   f"of {wl.name}; seconds/selection extrapolated by pair count"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="pages_512k", choices=sorted(W.BY_NAME))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-pairs", type=float, default=4.0e7,
+                    help="eligible pairs in the CPU oracle's timed row sample")
+    ap.add_argument("--ref-pairs-per-step", type=float, default=1.5e7)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    wl = W.BY_NAME[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        reference_arm(args, wl, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    kbuild.build()
+    K.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    inp = W.generate(wl, dev)
+    T, H, d = wl.total_tokens, wl.heads, wl.head_dim
+    B, Wd = wl.budget, wl.width
+    ids = torch.empty((T, B), dtype=torch.int32, device=dev)
+    toks = torch.empty((T, Wd), dtype=torch.int32, device=dev)
+    ws = K.new_workspace(T, wl.num_seqs, H, d, K.KPOOL_BF16 if wl.dtype == "bf16" else K.KPOOL_F32, wl.kpool,
+                         wl.index_topk, dev)
+    # five events per timed step, recorded by the library around its four kernels
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for evs in step_events:
+        for e in evs:
+            e.record(stream)
+    events = step_events[0]
+    pairs = wl.causal_pairs()
+    flops = FLOP_PER_PAIR_PER_HEAD_DIM * H * d * pairs
+
+    def step(ev=None):
+        K.kpool_select_ex(inp["q"], inp["k"], inp["w"], inp["cu_seqlens"], wl.kpool, wl.index_topk, wl.scale,
+                          out_pool_ids=ids, out_token_ids=toks, workspace=ws, stream=stream, stage_events=ev)
+
+    for _ in range(args.warmup):
+        step(events)
+    torch.cuda.synchronize()
+    st = K.kpool_last_device_error(ws)
+    if st != K.KPOOL_OK:
+        raise K.KpoolError(st, "device")
+
+    # ---- timed region: inputs resident in HBM (q alone is far larger than L2)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s_i in range(args.steps):
+        step(step_events[s_i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    per_kernel = [[evs[i].elapsed_time(evs[i + 1]) for evs in step_events] for i in range(4)]
+    barrier(world)
+    clock_info = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_step = max_over_ranks(ms_total / args.steps, world)
+    st = K.kpool_last_device_error(ws)
+    if st != K.KPOOL_OK:
+        raise K.KpoolError(st, "device")
+    value = world * pairs / (ms_step / 1e3)
+    k_ms = [statistics.mean(x) for x in per_kernel]
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
+        for k in h_in:
+            h_in[k].copy_(inp[k])
+        d_in = {k: torch.empty_like(v) for k, v in inp.items()}
+        h_ids = torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True)
+        h_toks = torch.empty(toks.shape, dtype=toks.dtype, pin_memory=True)
+        bi = sum(v.numel() * v.element_size() for v in h_in.values())
+        bo = h_ids.numel() * 4 + h_toks.numel() * 4
+
+        def e2e_step():
+            for k in d_in:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+            K.kpool_select_ex(d_in["q"], d_in["k"], d_in["w"], d_in["cu_seqlens"], wl.kpool, wl.index_topk,
+                              wl.scale, out_pool_ids=ids, out_token_ids=toks, workspace=ws, stream=stream)
+            h_ids.copy_(ids, non_blocking=True)
+            h_toks.copy_(toks, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world)
+        e2e = {"value": world * pairs / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+        del d_in, h_in
+
+    peaks = measured_peaks()
+    peak_sust = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    k2_s = k_ms[2] / 1e3
+    achieved = flops / k2_s / 1e12
+    tc_src = os.path.join(ROOT, "sparse_attention_kpool_gb300", "csrc", "kpool_select_tc.cu")
+    traffic = None
+    if NCU_TRAFFIC["kernel_sha256"] == source_sha(tc_src) and NCU_TRAFFIC["workload"] == wl.name:
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    hbm = float(peaks["hbm_gbs"])
+    kp_bytes = wl.num_pools() * d * 2
+    k1_bytes = T * d * 2 + kp_bytes
+    k3_bytes = T * B * 4 + T * Wd * 4
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "seqlens": list(wl.seqlens) if len(wl.seqlens) <= 8 else wl.num_seqs,
+                   "heads": H, "head_dim": d, "kpool": wl.kpool, "index_topk": wl.index_topk, "budget": B,
+                   "scale": wl.scale, "inputs": "q,k bf16 N(0,1), w fp32 U(0,1), seeded (CUDA Philox)",
+                   "l2": "inputs larger than L2 (q alone is %.1f GiB)" % (inp["q"].numel() * 2 / 2**30),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "sec_per_selection": ms_step / 1e3,
+        "scored_pairs_per_s": value,
+        "pct_bf16_peak": 100.0 * achieved / peak_sust,
+        "kernel_ms": {"plan": k_ms[0], "pool": k_ms[1], "score_select": k_ms[2], "expand": k_ms[3]},
+        "roofline": {"kernel": "select_tc_kernel (score+select)", "bound": "tensor", "achieved": achieved,
+                     "peak": peak_sust, "unit": "TFLOP/s", "frac": achieved / peak_sust, "traffic": traffic,
+                     "peak_kind": f"bf16 sustained, {peaks['_source']}",
+                     "frac_of_burst": achieved / float(peaks["bf16_tflops"]),
+                     "algorithmic_flop_per_launch": flops},
+        "hbm_kernels": {
+            "pool": {"bytes": k1_bytes, "GB/s": k1_bytes / (k_ms[1] / 1e3) / 1e9,
+                     "frac": k1_bytes / (k_ms[1] / 1e3) / 1e9 / hbm},
+            "expand": {"bytes": k3_bytes, "GB/s": k3_bytes / (k_ms[3] / 1e3) / 1e9,
+                       "frac": k3_bytes / (k_ms[3] / 1e3) / 1e9 / hbm}},
+        "clocks": clock_info,
+        "gpu_launches": 4 * args.steps,
+        "e2e": e2e,
+    }
+
+    if rank == 0 and not args.no_cpu:
+        rows = pick_sample_rows(wl, args.cpu_sample_pairs, seed=7)
+        res = oracle_sample(inp, wl, rows)
+        cpu_value = res["pairs"] / res["seconds"]
+        line["cpu_baseline"] = {
+            "value": cpu_value, "unit": UNIT, "cores": res["threads"], "kind": "oracle",
+            "sample": f"{len(rows)} uniform rows of {wl.name} ({res['pairs']:.3e} eligible pairs, "
+                      f"{res['seconds']:.1f} s incl. pooling all keys); fp64 scores",
+            "sec_per_selection_extrapolated": pairs / cpu_value}
+        # the same rows double as a parity spot check of this run's output
+        from tests import parity
+        r = torch.as_tensor(rows, device=dev)
+        sc_ids = ids[r].cpu().numpy()
+        ok = True
+        try:
+            parity.compare_float(inp, wl, dict(res["out"], rows=rows, kp=res["kp"]), sc_ids, None,
+                                 toks[r].cpu().numpy())
+        except AssertionError as ex:
+            ok = False
+            line["parity_sample_error"] = str(ex)[:200]
+        line["parity_sample"] = {"rows": int(len(rows)), "ok": ok}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -81,9 +81,13 @@ typedef enum {
 } kpool_score_kernel;
 
 typedef struct {
-  int32_t score_kernel;   /* a kpool_score_kernel value */
-  int32_t max_ctas;       /* 0: one persistent CTA per SM; > 0: cap (tests vary it) */
-  int32_t reserved[6];    /* must be zero */
+  int32_t score_kernel;       /* a kpool_score_kernel value */
+  int32_t max_ctas;           /* 0: one persistent CTA per SM; > 0: cap (tests vary it) */
+  void* const* stage_events;  /* NULL, or 5 cudaEvent_t (created by the caller) that are
+                                 recorded on `stream` before the planning kernel and after
+                                 the plan, pool, score+select and expand kernels, so a
+                                 caller can time each kernel without a profiler */
+  int32_t reserved[4];        /* must be zero */
 } kpool_options;
 
 /*

@@ -88,7 +88,7 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
                              const kpool_options* options) {
   kpool_options opt{};
   if (options) opt = *options;
-  for (int i = 0; i < 6; ++i)
+  for (int i = 0; i < 4; ++i)
     if (opt.reserved[i] != 0) return KPOOL_ERR_INVALID_ARG;
   if (opt.score_kernel < KPOOL_SCORE_AUTO || opt.score_kernel > KPOOL_SCORE_SIMT || opt.max_ctas < 0)
     return KPOOL_ERR_INVALID_ARG;
@@ -132,8 +132,14 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
   char* ws = static_cast<char*>(workspace);
   void* pooled = ws + L.pooled;
 
-  if (launch_plan(cu_seqlens, num_seqs, T, kpool, ws, L, stream) != cudaSuccess) return KPOOL_ERR_CUDA;
-  if (launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, pooled, ws, L, sms, stream) != cudaSuccess)
+  void* const* ev = opt.stage_events;
+  auto mark = [&](int i) {
+    return ev == nullptr || cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), stream) == cudaSuccess;
+  };
+  if (!mark(0)) return KPOOL_ERR_CUDA;
+  if (launch_plan(cu_seqlens, num_seqs, T, kpool, ws, L, stream) != cudaSuccess || !mark(1)) return KPOOL_ERR_CUDA;
+  if (launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, pooled, ws, L, sms, stream) != cudaSuccess ||
+      !mark(2))
     return KPOOL_ERR_CUDA;
   if (budget > 0) {
     cudaError_t e;
@@ -148,8 +154,10 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
     }
     if (e != cudaSuccess) return KPOOL_ERR_CUDA;
   }
+  if (!mark(3)) return KPOOL_ERR_CUDA;
   if (launch_expand(out_pool_ids, cu_seqlens, num_seqs, T, kpool, budget, out_token_ids,
-                    reinterpret_cast<const WorkspaceHeader*>(ws + L.header), sms, stream) != cudaSuccess)
+                    reinterpret_cast<const WorkspaceHeader*>(ws + L.header), sms, stream) != cudaSuccess ||
+      !mark(4))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
 }

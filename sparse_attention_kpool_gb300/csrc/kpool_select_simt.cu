@@ -18,33 +18,13 @@
 #include <cuda_bf16.h>
 
 #include "kpool_internal.cuh"
+#include "kpool_select_common.cuh"
 
 namespace kpool {
 namespace {
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// Descending bitonic sort of n (a power of two) keys in shared memory by one warp.
-__device__ void warp_sort_desc(uint64_t* buf, int n) {
-  const int lane = threadIdx.x & 31;
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = lane; i < n; i += 32) {
-        const int l = i ^ j;
-        if (l > i) {
-          const uint64_t a = buf[i], b = buf[l];
-          const bool desc = (i & k) == 0;
-          if (desc ? (a < b) : (a > b)) {
-            buf[i] = b;
-            buf[l] = a;
-          }
-        }
-      }
-      __syncwarp();
-    }
-  }
-}
 
 template <typename T, bool kNegScale>
 __global__ void __launch_bounds__(128) select_simt_kernel(

@@ -32,9 +32,11 @@
 //               tcgen05.ld -> relu, |scale|*w, head sum in fp32 -> selection key
 //               -> threshold filter -> candidate buffer in shared memory.
 // Selection: 1024 candidate slots per query row. A key enters only if it beats
-// the row's threshold (the budget-th best key kept so far). When a buffer passes
-// 896 entries the owning warp sorts it and cuts it back to `budget`, raising the
-// threshold. After the last tile it sorts once more and writes the ranked ids.
+// the row's threshold. When a buffer passes 896 entries its owning warp runs a
+// radix threshold search in registers and keeps between budget and budget+128
+// keys; the threshold rises to the search's edge. After the last tile the warp
+// cuts the buffer to exactly `budget` keys, sorts them in registers (bitonic)
+// and writes the ranked ids.
 //
 // Every mbarrier wait is bounded (poll count and ~1 s of wall time). A wait that
 // runs out records KPOOL_ERR_DEVICE_TIMEOUT in the workspace header; all roles
@@ -45,6 +47,7 @@
 
 #include "kpool_internal.cuh"
 #include "kpool_ptx.cuh"
+#include "kpool_select_common.cuh"
 
 namespace kpool {
 namespace {
@@ -58,6 +61,7 @@ constexpr int kStages = 3;
 constexpr int kCap = 1024;                // candidate slots per query row
 constexpr int kMaxBudget = 512;
 constexpr int kCompactAt = kCap - kTilePools;
+constexpr int kSlack = 128;               // a compaction keeps between budget and budget + kSlack keys
 constexpr int kThreads = 320;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
@@ -77,7 +81,8 @@ constexpr uint32_t kOffCount = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffTau = (kOffCount + kRows * 4 + 7) & ~7u;
 constexpr uint32_t kOffElig = kOffTau + kRows * 8;
 constexpr uint32_t kOffMisc = kOffElig + kRows * 4;
-constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kOffHist = kOffMisc + 16;                // 16 words per epilogue warp
+constexpr uint32_t kSmemUsed = kOffHist + 8 * 16 * 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
@@ -155,29 +160,8 @@ __device__ __forceinline__ Item load_item(const int2* items, const int32_t* cu, 
   return m;
 }
 
-// Descending bitonic sort of n (a power of two) keys in shared memory, one warp.
-__device__ void warp_sort_desc(uint64_t* buf, int n) {
-  const int lane = threadIdx.x & 31;
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = lane; i < n; i += 32) {
-        const int l = i ^ j;
-        if (l > i) {
-          const uint64_t a = buf[i], b = buf[l];
-          const bool desc = (i & k) == 0;
-          if (desc ? (a < b) : (a > b)) {
-            buf[i] = b;
-            buf[l] = a;
-          }
-        }
-      }
-      __syncwarp();
-    }
-  }
-}
-
 template <bool kNegScale>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
                      const float* __restrict__ w, const int32_t* __restrict__ cu,
                      const int32_t* __restrict__ pool_off, const int2* __restrict__ items,
@@ -194,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   int32_t* s_abort = reinterpret_cast<int32_t*>(smem + kOffMisc + 4);
   float* s_w = reinterpret_cast<float*>(smem + kOffW);
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
   uint64_t* s_cand = reinterpret_cast<uint64_t*>(smem + kOffCand);
 
   // n_items was written by the planning kernel before this launch and is 0 when
@@ -393,7 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int qq = 0; qq < 4; ++qq) {
             const int q = half * 4 + qq;
             const float4* wv = reinterpret_cast<const float4*>(s_w + q * kHeads);
-            float s = 0.0f;
+            // four independent partial sums (heads h = 4i + j go to sum j) keep the
+            // FMA chains short; they are added at the end
+            float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
 #pragma unroll
             for (int h4 = 0; h4 < kHeads / 4; ++h4) {
               const float4 ww = wv[h4];
@@ -401,11 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float x1 = __uint_as_float(v[qq][4 * h4 + 1]);
               const float x2 = __uint_as_float(v[qq][4 * h4 + 2]);
               const float x3 = __uint_as_float(v[qq][4 * h4 + 3]);
-              s = fmaf(ww.x, fmaxf(kNegScale ? -x0 : x0, 0.0f), s);
-              s = fmaf(ww.y, fmaxf(kNegScale ? -x1 : x1, 0.0f), s);
-              s = fmaf(ww.z, fmaxf(kNegScale ? -x2 : x2, 0.0f), s);
-              s = fmaf(ww.w, fmaxf(kNegScale ? -x3 : x3, 0.0f), s);
+              s0 = fmaf(ww.x, fmaxf(kNegScale ? -x0 : x0, 0.0f), s0);
+              s1 = fmaf(ww.y, fmaxf(kNegScale ? -x1 : x1, 0.0f), s1);
+              s2 = fmaf(ww.z, fmaxf(kNegScale ? -x2 : x2, 0.0f), s2);
+              s3 = fmaf(ww.w, fmaxf(kNegScale ? -x3 : x3, 0.0f), s3);
             }
+            const float s = (s0 + s1) + (s2 + s3);
             const uint64_t key = p < s_elig[q] ? make_key(s, uint32_t(p)) : 0ull;
             const bool pass = key > s_tau[q];
             const unsigned m = __ballot_sync(0xffffffffu, pass);
@@ -426,15 +414,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int q = half * 4 + wq;
           const int n = s_count[q];
           if (n > kCompactAt) {
-            uint64_t* buf = s_cand + q * kCap;
-            for (int e = n + lane; e < kCap; e += 32) buf[e] = 0;
-            __syncwarp();
-            warp_sort_desc(buf, kCap);
+            uint64_t edge;
+            const int kept = warp_select_compact<kCap / 32>(s_cand + q * kCap, n, budget, kSlack,
+                                                            s_hist + ew * 16, &edge);
             if (lane == 0) {
-              s_count[q] = budget;
-              s_tau[q] = buf[budget - 1];
+              s_count[q] = kept;
+              s_tau[q] = edge - 1;  // a key must reach the edge to matter from now on
             }
           }
+          __syncwarp();
         }
         named_bar(bar_id, 128);
         acc ^= 1;
@@ -446,18 +434,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = it.t0 + q;
         if (row < it.len) {
           uint64_t* buf = s_cand + q * kCap;
-          const int n = s_count[q];
-          int width = 32;
-          while (width < n) width <<= 1;
-          for (int e = n + lane; e < width; e += 32) buf[e] = 0;
-          __syncwarp();
-          warp_sort_desc(buf, width);
-          const int64_t grow = it.seq_start + row;
-          for (int j = lane; j < budget; j += 32) {
-            const uint64_t key = j < width ? buf[j] : 0ull;
-            out_ids[grow * budget + j] = key ? int32_t(key_pool(key)) : -1;
-            if (out_scores) out_scores[grow * budget + j] = key ? key_score(key) : -INFINITY;
+          int n = s_count[q];
+          if (n > budget) {  // cut to exactly the top `budget` (slack 0), unordered
+            uint64_t edge;
+            n = warp_select_compact<kCap / 32>(buf, n, budget, 0, s_hist + ew * 16, &edge);
           }
+          uint64_t k[kMaxBudget / 32];
+#pragma unroll
+          for (int r = 0; r < kMaxBudget / 32; ++r) {
+            const int e = 32 * r + lane;
+            k[r] = e < n ? buf[e] : 0ull;
+          }
+          warp_sort_regs_desc<kMaxBudget / 32>(k);
+          const int64_t grow = it.seq_start + row;
+#pragma unroll
+          for (int r = 0; r < kMaxBudget / 32; ++r) {
+            const int j = 32 * r + lane;
+            if (j < budget) {
+              out_ids[grow * budget + j] = k[r] ? int32_t(key_pool(k[r])) : -1;
+              if (out_scores) out_scores[grow * budget + j] = k[r] ? key_score(k[r]) : -INFINITY;
+            }
+          }
+          __syncwarp();
         }
       }
       named_bar(bar_id, 128);

@@ -48,7 +48,7 @@ class KpoolError(RuntimeError):
 
 class kpool_options(ctypes.Structure):
     _fields_ = [("score_kernel", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 6)]
+                ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("reserved", ctypes.c_int32 * 4)]
 
 
 _lib = None
@@ -137,9 +137,12 @@ def new_workspace(total_tokens: int, num_seqs: int, heads: int, head_dim: int, d
 def kpool_select_ex(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor, kpool: int,
                     index_topk: int, scale: float, out_pool_ids=None, out_token_ids=None, out_pool_scores=None,
                     return_scores: bool = False, workspace=None, stream=None, score_kernel: int = KPOOL_SCORE_AUTO,
-                    max_ctas: int = 0):
+                    max_ctas: int = 0, stage_events=None):
     """q [T,H,d], k [T,d] (bf16 or fp32), w [T,H] fp32, cu_seqlens [S+1] int32 -> (pool_ids [T,B],
-    token_ids [T, index_topk+kpool], pool_scores [T,B] or None)."""
+    token_ids [T, index_topk+kpool], pool_scores [T,B] or None).
+
+    stage_events: optional 5 already-recorded torch.cuda.Event(enable_timing=True); the library
+    re-records them around its four kernels (see kpool_options in kpool.h)."""
     T, H, d = q.shape
     S = cu_seqlens.numel() - 1
     dt = _dtype_code(q)
@@ -157,6 +160,13 @@ def kpool_select_ex(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, cu_seqlen
         workspace = new_workspace(T, S, H, d, dt, kpool, index_topk, dev)
     _check_cuda(q, k, w, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores, workspace)
     opts = kpool_options(score_kernel, max_ctas)
+    if stage_events is not None:
+        if len(stage_events) != 5:
+            raise ValueError("stage_events needs 5 events")
+        arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(int(e.cuda_event)) for e in stage_events])
+        if not all(arr):
+            raise ValueError("record each event once before passing it (torch creates events lazily)")
+        opts.stage_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
     st = load().kpool_select_ex(_ptr(q), _ptr(k), _ptr(w), _ptr(cu_seqlens), S, T, H, d, dt, kpool, index_topk,
                                 float(scale), _ptr(out_pool_ids), _ptr(out_token_ids), _ptr(out_pool_scores),
                                 _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts))

@@ -131,9 +131,9 @@ def _plant_duplicate_pools(k: torch.Tensor, cu: torch.Tensor, kpool: int, every:
     for b in range(len(cu) - 1):
         start, L = int(cu[b]), int(cu[b + 1] - cu[b])
         n = L // kpool
-        dst = torch.arange(every - 1, n, every)
-        if len(dst) == 0:
+        if n < every:
             continue
+        dst = torch.arange(every - 1, n, every)
         # draw src uniformly in [0, dst): floor(u * dst)
         u = torch.rand(len(dst), generator=g, dtype=torch.float64)
         src = torch.minimum((u * dst.to(torch.float64)).floor().to(torch.int64), dst - 1)

@@ -31,6 +31,10 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(kpool_[a-z_]+)\s*\(", text)))
 
 
+def test_options_struct_layout_matches_header():
+    assert ctypes.sizeof(K.kpool_options) == 32
+
+
 def test_header_declares_the_binding_names():
     assert declared_functions() == sorted(K.EXPORTED)
 
@@ -92,7 +96,7 @@ def test_select_rejects_bad_arguments(lib):
     assert _select(lib, ws=FAKE + 64) == K.KPOOL_ERR_WORKSPACE     # 256-byte alignment
     assert _select(lib, ws_bytes=1024) == K.KPOOL_ERR_WORKSPACE
     bad = K.kpool_options(K.KPOOL_SCORE_AUTO, 0)
-    bad.reserved[2] = 1
+    bad.reserved[3] = 1
     assert _select(lib, opts=bad) == K.KPOOL_ERR_INVALID_ARG
     assert _select(lib, opts=K.kpool_options(9, 0)) == K.KPOOL_ERR_INVALID_ARG
     assert _select(lib, opts=K.kpool_options(0, -1)) == K.KPOOL_ERR_INVALID_ARG
