@@ -160,6 +160,12 @@ kpool_status kpool_wait_timeout_selftest(void* workspace, size_t workspace_bytes
 /* Static, human-readable name of a status code. */
 const char* kpool_status_string(kpool_status status);
 
+/*
+ * Name of the CUDA error behind the most recent KPOOL_ERR_CUDA returned to the
+ * calling host thread ("cudaSuccess" if none). Static string; never touches the GPU.
+ */
+const char* kpool_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,6 +14,14 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices] = {0};
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// Remembers a failing CUDA call for kpool_last_cuda_error and maps it to a status.
+bool cuda_ok(cudaError_t e) {
+  if (e == cudaSuccess) return true;
+  g_last_cuda_error = e;
+  return false;
+}
 
 cudaError_t sm_count(int* out) {
   int dev = 0;
@@ -128,17 +136,17 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int sms = 0;
-  if (sm_count(&sms) != cudaSuccess) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
   void* pooled = ws + L.pooled;
 
   void* const* ev = opt.stage_events;
   auto mark = [&](int i) {
-    return ev == nullptr || cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), stream) == cudaSuccess;
+    return ev == nullptr || cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), stream));
   };
   if (!mark(0)) return KPOOL_ERR_CUDA;
-  if (launch_plan(cu_seqlens, num_seqs, T, kpool, ws, L, stream) != cudaSuccess || !mark(1)) return KPOOL_ERR_CUDA;
-  if (launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, pooled, ws, L, sms, stream) != cudaSuccess ||
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, T, kpool, ws, L, stream)) || !mark(1)) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, pooled, ws, L, sms, stream)) ||
       !mark(2))
     return KPOOL_ERR_CUDA;
   if (budget > 0) {
@@ -152,11 +160,11 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
       e = launch_select_simt(q, pooled, w, dtype, cu_seqlens, num_seqs, T, heads, head_dim, kpool, budget, scale,
                              out_pool_ids, out_pool_scores, ws, L, opt.max_ctas > 0 ? opt.max_ctas : sms, stream);
     }
-    if (e != cudaSuccess) return KPOOL_ERR_CUDA;
+    if (!cuda_ok(e)) return KPOOL_ERR_CUDA;
   }
   if (!mark(3)) return KPOOL_ERR_CUDA;
-  if (launch_expand(out_pool_ids, cu_seqlens, num_seqs, T, kpool, budget, out_token_ids,
-                    reinterpret_cast<const WorkspaceHeader*>(ws + L.header), sms, stream) != cudaSuccess ||
+  if (!cuda_ok(launch_expand(out_pool_ids, cu_seqlens, num_seqs, T, kpool, budget, out_token_ids,
+                             reinterpret_cast<const WorkspaceHeader*>(ws + L.header), sms, stream)) ||
       !mark(4))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
@@ -185,11 +193,11 @@ kpool_status kpool_pool_keys(const void* k, const int32_t* cu_seqlens, int32_t n
   if (st != KPOOL_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int sms = 0;
-  if (sm_count(&sms) != cudaSuccess) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  if (launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, ws, L, stream) != cudaSuccess) return KPOOL_ERR_CUDA;
-  if (launch_pool(k, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool, out_pooled_keys, ws, L, sms,
-                  stream) != cudaSuccess)
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, ws, L, stream))) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool, out_pooled_keys, ws, L,
+                           sms, stream)))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
 }
@@ -205,9 +213,9 @@ kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, in
   if (!cu_seqlens || !out_token_ids || (budget > 0 && !pool_ids)) return KPOOL_ERR_INVALID_ARG;
   if (!aligned(pool_ids, 4) || !aligned(out_token_ids, 4) || !aligned(cu_seqlens, 4)) return KPOOL_ERR_INVALID_ARG;
   int sms = 0;
-  if (sm_count(&sms) != cudaSuccess) return KPOOL_ERR_CUDA;
-  if (launch_expand(pool_ids, cu_seqlens, num_seqs, total_tokens, kpool, budget, out_token_ids, nullptr, sms,
-                    static_cast<cudaStream_t>(stream_ptr)) != cudaSuccess)
+  if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_expand(pool_ids, cu_seqlens, num_seqs, total_tokens, kpool, budget, out_token_ids, nullptr,
+                             sms, static_cast<cudaStream_t>(stream_ptr))))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
 }
@@ -215,9 +223,9 @@ kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, in
 kpool_status kpool_last_device_error(const void* workspace, void* stream_ptr) {
   if (workspace == nullptr || !aligned(workspace, 256)) return KPOOL_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(cudaStreamSynchronize(stream))) return KPOOL_ERR_CUDA;
   int32_t code = 0;
-  if (cudaMemcpy(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(cudaMemcpy(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost))) return KPOOL_ERR_CUDA;
   if (code < 0 || code > KPOOL_ERR_DEVICE_TIMEOUT) return KPOOL_ERR_CUDA;
   return static_cast<kpool_status>(code);
 }
@@ -227,8 +235,8 @@ kpool_status kpool_wait_timeout_selftest(void* workspace, size_t workspace_bytes
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < sizeof(WorkspaceHeader))
     return KPOOL_ERR_WORKSPACE;
   if (spin_limit < 1) return KPOOL_ERR_INVALID_ARG;
-  if (launch_wait_selftest(static_cast<char*>(workspace), spin_limit, static_cast<cudaStream_t>(stream_ptr)) !=
-      cudaSuccess)
+  if (!cuda_ok(launch_wait_selftest(static_cast<char*>(workspace), spin_limit,
+                                    static_cast<cudaStream_t>(stream_ptr))))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
 }
@@ -244,5 +252,7 @@ const char* kpool_status_string(kpool_status status) {
   }
   return "unknown status";
 }
+
+const char* kpool_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 }  // extern "C"

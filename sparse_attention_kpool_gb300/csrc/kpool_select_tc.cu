@@ -161,7 +161,7 @@ __device__ __forceinline__ Item load_item(const int2* items, const int32_t* cu, 
 }
 
 template <bool kNegScale>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
                      const float* __restrict__ w, const int32_t* __restrict__ cu,
                      const int32_t* __restrict__ pool_off, const int2* __restrict__ items,

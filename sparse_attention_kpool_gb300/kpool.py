@@ -36,14 +36,15 @@ KPOOL_SCORE_SIMT = 2
 
 EXPORTED = (
     "kpool_workspace_bytes", "kpool_select", "kpool_select_ex", "kpool_pool_keys", "kpool_expand",
-    "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string",
+    "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string", "kpool_last_cuda_error",
 )
 
 
 class KpoolError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {kpool_status_string(status)} (status {status})")
+        detail = f" [{kpool_last_cuda_error()}]" if status == KPOOL_ERR_CUDA else ""
+        super().__init__(f"{what}: {kpool_status_string(status)} (status {status}){detail}")
 
 
 class kpool_options(ctypes.Structure):
@@ -87,12 +88,18 @@ def load() -> ctypes.CDLL:
         lib.kpool_wait_timeout_selftest.restype = i32
         lib.kpool_status_string.argtypes = [i32]
         lib.kpool_status_string.restype = ctypes.c_char_p
+        lib.kpool_last_cuda_error.argtypes = []
+        lib.kpool_last_cuda_error.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
 
 def kpool_status_string(status: int) -> str:
     return load().kpool_status_string(int(status)).decode()
+
+
+def kpool_last_cuda_error() -> str:
+    return load().kpool_last_cuda_error().decode()
 
 
 def _dtype_code(t: torch.Tensor) -> int:
