@@ -157,6 +157,40 @@ kpool_status kpool_last_device_error(const void* workspace, void* stream);
 kpool_status kpool_wait_timeout_selftest(void* workspace, size_t workspace_bytes, int64_t spin_limit,
                                          void* stream);
 
+/*
+ * Capacity of the library's built-in scratch array used by
+ * kpool_select_static_scratch: 48 MiB, enough for one batch of about 750,000
+ * tokens at kpool 4, d 128, bf16 (kpool_workspace_bytes() <= this value).
+ */
+#define KPOOL_STATIC_SCRATCH_BYTES ((size_t)48 << 20)
+
+/*
+ * kpool_select for callers that cannot allocate device memory. The pages have
+ * no counterpart to this entry point; it exists for callers such as a plugin or
+ * custom operator inside a framework that owns all device memory, or a
+ * real-time path that must never pay cudaMalloc's implicit synchronisation,
+ * which have no workspace to pass. It runs the same kernels as kpool_select with
+ * the scratch taken from a file-scope __device__ array of
+ * KPOOL_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits. Inputs and outputs are still the caller's device buffers.
+ *   - A call whose kpool_workspace_bytes(...) exceeds KPOOL_STATIC_SCRATCH_BYTES
+ *     returns KPOOL_ERR_WORKSPACE before any GPU work.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current) and caches it: make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents: calls that overlap on the GPU race and must be serialised.
+ *   - It allocates nothing (no cudaMalloc/cudaFree or allocating library call).
+ *   - Device-side errors land in the shared array's header, which the caller
+ *     cannot name, so they are not reported (malformed cu_seqlens leaves the
+ *     outputs unwritten, as with kpool_select).
+ */
+kpool_status kpool_select_static_scratch(const void* q, const void* k, const float* w,
+                                         const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                         int32_t heads, int32_t head_dim, kpool_dtype dtype, int32_t kpool,
+                                         int32_t index_topk, float scale, int32_t* out_pool_ids,
+                                         int32_t* out_token_ids, float* out_pool_scores, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* kpool_status_string(kpool_status status);
 

@@ -37,7 +37,9 @@ KPOOL_SCORE_SIMT = 2
 EXPORTED = (
     "kpool_workspace_bytes", "kpool_select", "kpool_select_ex", "kpool_pool_keys", "kpool_expand",
     "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string", "kpool_last_cuda_error",
+    "kpool_select_static_scratch",
 )
+KPOOL_STATIC_SCRATCH_BYTES = 48 << 20
 
 
 class KpoolError(RuntimeError):
@@ -90,6 +92,8 @@ def load() -> ctypes.CDLL:
         lib.kpool_status_string.restype = ctypes.c_char_p
         lib.kpool_last_cuda_error.argtypes = []
         lib.kpool_last_cuda_error.restype = ctypes.c_char_p
+        lib.kpool_select_static_scratch.argtypes = [P, P, P, P, i32, i64, i32, i32, i32, i32, i32, f32, P, P, P, P]
+        lib.kpool_select_static_scratch.restype = i32
         _lib = lib
         return lib
 
@@ -226,3 +230,29 @@ def kpool_last_device_error(workspace: torch.Tensor, stream=None) -> int:
 def kpool_wait_timeout_selftest(workspace: torch.Tensor, spin_limit: int, stream=None) -> int:
     return int(load().kpool_wait_timeout_selftest(_ptr(workspace), workspace.numel(), int(spin_limit),
                                                   _stream(stream)))
+
+
+def kpool_select_static_scratch(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor,
+                                kpool: int, index_topk: int, scale: float, out_pool_ids=None, out_token_ids=None,
+                                out_pool_scores=None, return_scores: bool = False, stream=None):
+    """kpool_select with the library's built-in scratch array instead of a workspace (for callers
+    that cannot allocate device memory; see kpool_select_static_scratch in kpool.h). The outputs
+    are allocated here only when not passed."""
+    T, H, d = q.shape
+    S = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    B = index_topk // kpool if kpool > 0 else 0
+    dev = q.device
+    if out_pool_ids is None:
+        out_pool_ids = torch.empty((T, B), dtype=torch.int32, device=dev)
+    if out_token_ids is None:
+        out_token_ids = torch.empty((T, index_topk + kpool), dtype=torch.int32, device=dev)
+    if out_pool_scores is None and return_scores:
+        out_pool_scores = torch.empty((T, B), dtype=torch.float32, device=dev)
+    _check_cuda(q, k, w, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores)
+    st = load().kpool_select_static_scratch(_ptr(q), _ptr(k), _ptr(w), _ptr(cu_seqlens), S, T, H, d, dt, kpool,
+                                            index_topk, float(scale), _ptr(out_pool_ids), _ptr(out_token_ids),
+                                            _ptr(out_pool_scores), _stream(stream))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_select_static_scratch")
+    return out_pool_ids, out_token_ids, out_pool_scores
