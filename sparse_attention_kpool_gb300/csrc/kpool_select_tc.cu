@@ -27,9 +27,11 @@
 //               3-stage ring (32 KB each).
 //   warp 1      TMEM owner and MMA issuer: two 256-column accumulators, so the
 //               epilogue drains one while the tensor core fills the other.
-//   warps 2..9  epilogue, two groups of four warps (queries 0-3 and 4-7 of the
-//               item); warp w reads TMEM lanes 32*(w%4).. (the hardware rule).
-//               tcgen05.ld -> relu, |scale|*w, head sum in fp32 -> selection key
+//   warps 2..9  epilogue, two groups of four warps in ping-pong: group g drains
+//               accumulator g (every other tile) for all 8 rows, so one group's
+//               TMEM/atomic latency overlaps the other's arithmetic; warp w reads
+//               TMEM lanes 32*(w%4).. (the hardware rule). tcgen05.ld -> relu,
+//               |scale|*w, head sum in fp32 (packed f32x2 FMAs) -> selection key
 //               -> threshold filter -> candidate buffer in shared memory.
 // Selection: 1024 candidate slots per query row. A key enters only if it beats
 // the row's threshold. When a buffer passes 896 entries its owning warp runs a
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar.acc_full + a, 1);
-      ptx::mbar_init(bar.acc_empty + a, 8);
+      ptx::mbar_init(bar.acc_empty + a, 4);
     }
     ptx::mbar_init(bar.mma_done, 1);
     ptx::fence_mbar_init();
@@ -325,140 +327,157 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;          // 0..7
-    const int half = ew >> 2;         // which four query rows of the item
-    const int wq = ew & 3;            // this warp's query row within the half (for selection work)
+    // Ping-pong: group `grp` (warps 2-5 -> 0, warps 6-9 -> 1) drains accumulator grp,
+    // i.e. every other tile of the CTA's global tile sequence, for all 8 rows of the
+    // item; while one group waits on TMEM or on its atomics the other computes.
+    const int ew = warp - 2;          // 0..7, also the item row this warp ranks and compacts
+    const int grp = ew >> 2;          // accumulator this group drains
     const int lg = warp & 3;          // TMEM lane group this warp may read
-    const int tw = wq * 32 + lane;    // thread index within the group of four warps
-    const int bar_id = 1 + half;
+    const int et = ew * 32 + lane;    // thread index among the 256 epilogue threads
     const unsigned lt_mask = (1u << lane) - 1u;
-    const uint32_t lane_addr = tmem_base + (uint32_t(lg * 32) << 16);
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    const uint32_t lane_addr = tmem_base + (uint32_t(lg * 32) << 16) + uint32_t(grp * kAccCols);
+    uint32_t phase = 0;               // next phase of acc_full[grp] this group consumes
+    uint32_t g = 0;                   // tiles of this CTA before the current item
     for (int r = 0;; ++r) {
       const int idx = item_index(r, blockIdx.x, gridDim.x);
       if (idx >= n_items) break;
       const Item it = load_item(items, cu, pool_off, idx, kpool);
-      // per-item state of this half's four rows
-      for (int e = tw; e < 4 * kHeads; e += 128) {
-        const int qq = e / kHeads, h = e % kHeads;
-        const int row = it.t0 + half * 4 + qq;
-        s_w[(half * 4 + qq) * kHeads + h] =
-            row < it.len ? w[(it.seq_start + row) * kHeads + h] * abs_scale : 0.0f;
-      }
-      if (tw < 4) {
-        const int q = half * 4 + tw;
+      // per-item state of the 8 rows
+      for (int e = et; e < kRows * kHeads; e += 256) {
+        const int q = e / kHeads, h = e % kHeads;
         const int row = it.t0 + q;
-        s_count[q] = 0;
-        s_tau[q] = 0;
-        s_elig[q] = row < it.len ? (row + 1) / kpool : 0;
+        s_w[e] = row < it.len ? w[(it.seq_start + row) * kHeads + h] * abs_scale : 0.0f;
       }
-      named_bar(bar_id, 128);
+      if (et < kRows) {
+        const int row = it.t0 + et;
+        s_count[et] = 0;
+        s_tau[et] = 0;
+        s_elig[et] = row < it.len ? (row + 1) / kpool : 0;
+      }
+      named_bar(1, 256);
       bool aborted = false;
-      for (int i = 0; i < it.n_tiles; ++i) {
+      // round k pairs local tile 2k - (g&1) (group 0) with 2k - (g&1) + 1 (group 1)
+      const int n_rounds = it.n_tiles > 0 ? ((int(g & 1) + it.n_tiles - 1) >> 1) + 1 : 0;
+      for (int k = 0; k < n_rounds; ++k) {
+        const int t = 2 * k - int(g & 1) + grp;  // this group's local tile in the round
+        const bool has = t >= 0 && t < it.n_tiles;
         bool ready = true;
-        if (lane == 0) ready = ptx::mbar_wait_bounded(bar.acc_full + acc, acc_phase, kMaxPolls, kMaxWaitNs);
-        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-        if (!ready) {
-          record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
-          *abort_flag = 1;
-        }
-        if (ready) {
-          ptx::tc_fence_after();
-          uint32_t v[4][32];
+        bool over = false;  // a reservation of this warp pushed a row past the compaction mark
+        if (has) {
+          if (lane == 0) ready = ptx::mbar_wait_bounded(bar.acc_full + grp, phase, kMaxPolls, kMaxWaitNs);
+          ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+          if (!ready) {
+            record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+          } else {
+            phase ^= 1;
+            ptx::tc_fence_after();
+            const int p = t * kTilePools + lg * 32 + lane;  // sequence-local pool index of this thread
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq)
-            ptx::tc_ld_32x32b_x32(lane_addr + uint32_t(acc * kAccCols + (half * 4 + qq) * kHeads), v[qq]);
-          ptx::tc_wait_ld();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar.acc_empty + acc);
-          const int p = i * kTilePools + lg * 32 + lane;  // sequence-local pool index of this thread
+            for (int bq = 0; bq < 2; ++bq) {  // rows 4bq .. 4bq+3
+              uint32_t v[4][32];
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const int q = half * 4 + qq;
-            const float4* wv = reinterpret_cast<const float4*>(s_w + q * kHeads);
-            // four independent partial sums (heads h = 4i + j go to sum j) keep the
-            // FMA chains short; they are added at the end
-            float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+              for (int qq = 0; qq < 4; ++qq)
+                ptx::tc_ld_32x32b_x32(lane_addr + uint32_t((4 * bq + qq) * kHeads), v[qq]);
+              ptx::tc_wait_ld();
+              if (bq == 1) {  // every column is in registers: hand the accumulator back
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar.acc_empty + grp);
+              }
+              uint64_t key[4];
+              unsigned m[4];
 #pragma unroll
-            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-              const float4 ww = wv[h4];
-              const float x0 = __uint_as_float(v[qq][4 * h4 + 0]);
-              const float x1 = __uint_as_float(v[qq][4 * h4 + 1]);
-              const float x2 = __uint_as_float(v[qq][4 * h4 + 2]);
-              const float x3 = __uint_as_float(v[qq][4 * h4 + 3]);
-              s0 = fmaf(ww.x, fmaxf(kNegScale ? -x0 : x0, 0.0f), s0);
-              s1 = fmaf(ww.y, fmaxf(kNegScale ? -x1 : x1, 0.0f), s1);
-              s2 = fmaf(ww.z, fmaxf(kNegScale ? -x2 : x2, 0.0f), s2);
-              s3 = fmaf(ww.w, fmaxf(kNegScale ? -x3 : x3, 0.0f), s3);
-            }
-            const float s = (s0 + s1) + (s2 + s3);
-            const uint64_t key = p < s_elig[q] ? make_key(s, uint32_t(p)) : 0ull;
-            const bool pass = key > s_tau[q];
-            const unsigned m = __ballot_sync(0xffffffffu, pass);
-            if (m) {
-              const int leader = __ffs(m) - 1;
+              for (int qq = 0; qq < 4; ++qq) {
+                const int q = 4 * bq + qq;
+                const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + q * kHeads);
+                // heads 4i, 4i+1 accumulate in acc0 and 4i+2, 4i+3 in acc1 (four partial
+                // sums, two fp32 lanes each), added at the end
+                uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+                for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+                  const ulonglong2 ww = wv[h4];
+                  const float x0 = __uint_as_float(v[qq][4 * h4 + 0]);
+                  const float x1 = __uint_as_float(v[qq][4 * h4 + 1]);
+                  const float x2 = __uint_as_float(v[qq][4 * h4 + 2]);
+                  const float x3 = __uint_as_float(v[qq][4 * h4 + 3]);
+                  acc0 = ptx::fma_f32x2(ww.x, ptx::pack_f32x2(fmaxf(kNegScale ? -x0 : x0, 0.0f),
+                                                              fmaxf(kNegScale ? -x1 : x1, 0.0f)), acc0);
+                  acc1 = ptx::fma_f32x2(ww.y, ptx::pack_f32x2(fmaxf(kNegScale ? -x2 : x2, 0.0f),
+                                                              fmaxf(kNegScale ? -x3 : x3, 0.0f)), acc1);
+                }
+                float s0, s1, s2, s3;
+                ptx::unpack_f32x2(acc0, s0, s1);
+                ptx::unpack_f32x2(acc1, s2, s3);
+                const float s = (s0 + s1) + (s2 + s3);
+                key[qq] = p < s_elig[q] ? make_key(s, uint32_t(p)) : 0ull;
+                m[qq] = __ballot_sync(0xffffffffu, key[qq] > s_tau[q]);
+              }
+              // lanes 0..3 reserve buffer slots for the four rows with one shared atomic
+              const unsigned my_m = lane == 0 ? m[0] : lane == 1 ? m[1] : lane == 2 ? m[2] : m[3];
               int base = 0;
-              if (lane == leader) base = atomicAdd(s_count + q, __popc(m));
-              base = __shfl_sync(0xffffffffu, base, leader);
-              if (pass) s_cand[q * kCap + base + __popc(m & lt_mask)] = key;
+              if (lane < 4 && my_m != 0) base = atomicAdd(s_count + 4 * bq + lane, __popc(my_m));
+              over = over || (lane < 4 && base + __popc(my_m) > kCompactAt);
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                const int b = __shfl_sync(0xffffffffu, base, qq);
+                if ((m[qq] >> lane) & 1u) s_cand[(4 * bq + qq) * kCap + b + __popc(m[qq] & lt_mask)] = key[qq];
+              }
             }
           }
         }
-        if (named_bar_or(bar_id, 128, !ready || *abort_flag != 0)) {
-          aborted = true;
-          break;
-        }
-        {  // keep the candidate buffer of this warp's row below the compaction mark
-          const int q = half * 4 + wq;
-          const int n = s_count[q];
+        // one barrier per round in the common case; its OR says whether any row needs
+        // compacting or a wait ran out
+        if (named_bar_or(1, 256, over || !ready || *abort_flag != 0)) {
+          if (named_bar_or(1, 256, !ready || *abort_flag != 0)) {
+            aborted = true;
+            break;
+          }
+          const int n = s_count[ew];  // warp ew brings row ew back below the compaction mark
           if (n > kCompactAt) {
             uint64_t edge;
-            const int kept = warp_select_compact<kCap / 32>(s_cand + q * kCap, n, budget, kSlack,
+            const int kept = warp_select_compact<kCap / 32>(s_cand + ew * kCap, n, budget, kSlack,
                                                             s_hist + ew * 16, &edge);
             if (lane == 0) {
-              s_count[q] = kept;
-              s_tau[q] = edge - 1;  // a key must reach the edge to matter from now on
+              s_count[ew] = kept;
+              s_tau[ew] = edge - 1;  // a key must reach the edge to matter from now on
             }
           }
           __syncwarp();
+          named_bar(1, 256);
         }
-        named_bar(bar_id, 128);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
       }
       if (aborted) break;
-      {  // final ranking of this warp's row
-        const int q = half * 4 + wq;
-        const int row = it.t0 + q;
+      g += uint32_t(it.n_tiles);
+      {  // final ranking of row ew
+        const int row = it.t0 + ew;
         if (row < it.len) {
-          uint64_t* buf = s_cand + q * kCap;
-          int n = s_count[q];
+          uint64_t* buf = s_cand + ew * kCap;
+          int n = s_count[ew];
           if (n > budget) {  // cut to exactly the top `budget` (slack 0), unordered
             uint64_t edge;
             n = warp_select_compact<kCap / 32>(buf, n, budget, 0, s_hist + ew * 16, &edge);
           }
-          uint64_t k[kMaxBudget / 32];
+          uint64_t kk[kMaxBudget / 32];
 #pragma unroll
-          for (int r = 0; r < kMaxBudget / 32; ++r) {
-            const int e = 32 * r + lane;
-            k[r] = e < n ? buf[e] : 0ull;
+          for (int j = 0; j < kMaxBudget / 32; ++j) {
+            const int e = 32 * j + lane;
+            kk[j] = e < n ? buf[e] : 0ull;
           }
-          warp_sort_regs_desc<kMaxBudget / 32>(k);
+          warp_sort_regs_desc<kMaxBudget / 32>(kk);
           const int64_t grow = it.seq_start + row;
 #pragma unroll
-          for (int r = 0; r < kMaxBudget / 32; ++r) {
-            const int j = 32 * r + lane;
-            if (j < budget) {
-              out_ids[grow * budget + j] = k[r] ? int32_t(key_pool(k[r])) : -1;
-              if (out_scores) out_scores[grow * budget + j] = k[r] ? key_score(k[r]) : -INFINITY;
+          for (int j = 0; j < kMaxBudget / 32; ++j) {
+            const int o = 32 * j + lane;
+            if (o < budget) {
+              out_ids[grow * budget + o] = kk[j] ? int32_t(key_pool(kk[j])) : -1;
+              if (out_scores) out_scores[grow * budget + o] = kk[j] ? key_score(kk[j]) : -INFINITY;
             }
           }
           __syncwarp();
         }
       }
-      named_bar(bar_id, 128);
+      named_bar(1, 256);
     }
     ptx::tc_fence_before();
   }
