@@ -68,7 +68,9 @@ typedef enum {
   KPOOL_ERR_UNSUPPORTED = 2,    /* shape outside what the kernels implement */
   KPOOL_ERR_WORKSPACE = 3,      /* workspace null, misaligned or too small */
   KPOOL_ERR_CUDA = 4,           /* a CUDA runtime/driver call or launch failed */
-  KPOOL_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait ran out */
+  KPOOL_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait ran out */
+  KPOOL_ERR_INTERNAL = 6        /* a device-side bounds guard fired (a library bug; the
+                                   offending write was skipped) */
 } kpool_status;
 
 typedef enum { KPOOL_BF16 = 0, KPOOL_F32 = 1 } kpool_dtype;
@@ -142,8 +144,8 @@ kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, in
 /*
  * Synchronises `stream`, then reads the device error word the last call on this
  * workspace recorded: KPOOL_OK, KPOOL_ERR_INVALID_ARG (malformed cu_seqlens),
- * KPOOL_ERR_DEVICE_TIMEOUT (a bounded wait ran out), or KPOOL_ERR_CUDA if the
- * synchronisation or copy itself failed.
+ * KPOOL_ERR_DEVICE_TIMEOUT (a bounded wait ran out), KPOOL_ERR_INTERNAL (a
+ * bounds guard fired), or KPOOL_ERR_CUDA if the synchronisation or copy failed.
  */
 kpool_status kpool_last_device_error(const void* workspace, void* stream);
 

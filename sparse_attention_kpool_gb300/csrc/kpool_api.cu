@@ -226,7 +226,7 @@ kpool_status kpool_last_device_error(const void* workspace, void* stream_ptr) {
   if (!cuda_ok(cudaStreamSynchronize(stream))) return KPOOL_ERR_CUDA;
   int32_t code = 0;
   if (!cuda_ok(cudaMemcpy(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost))) return KPOOL_ERR_CUDA;
-  if (code < 0 || code > KPOOL_ERR_DEVICE_TIMEOUT) return KPOOL_ERR_CUDA;
+  if (code < 0 || code > KPOOL_ERR_INTERNAL) return KPOOL_ERR_CUDA;
   return static_cast<kpool_status>(code);
 }
 
@@ -249,6 +249,7 @@ const char* kpool_status_string(kpool_status status) {
     case KPOOL_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case KPOOL_ERR_CUDA: return "CUDA error";
     case KPOOL_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case KPOOL_ERR_INTERNAL: return "device-side bounds guard fired";
   }
   return "unknown status";
 }

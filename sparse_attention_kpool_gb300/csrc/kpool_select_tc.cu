@@ -34,8 +34,8 @@
 //               |scale|*w, head sum in fp32 (packed f32x2 FMAs) -> selection key
 //               -> threshold filter -> candidate buffer in shared memory.
 // Selection: 1024 candidate slots per query row. A key enters only if it beats
-// the row's threshold. When a buffer passes 896 entries its owning warp runs a
-// radix threshold search in registers and keeps between budget and budget+128
+// the row's threshold. When a buffer passes 768 entries its owning warp runs a
+// radix threshold search in registers and keeps between budget and budget+64
 // keys; the threshold rises to the search's edge. After the last tile the warp
 // cuts the buffer to exactly `budget` keys, sorts them in registers (bitonic)
 // and writes the ranked ids.
@@ -62,8 +62,11 @@ constexpr int kTilePools = 128;           // MMA M
 constexpr int kStages = 3;
 constexpr int kCap = 1024;                // candidate slots per query row
 constexpr int kMaxBudget = 512;
-constexpr int kCompactAt = kCap - kTilePools;
-constexpr int kSlack = 128;               // a compaction keeps between budget and budget + kSlack keys
+// A barrier round covers two tiles (one per epilogue group), i.e. up to 256 new
+// candidates per row, so a row is compacted once it holds more than kCap - 256.
+constexpr int kCompactAt = kCap - 2 * kTilePools;
+constexpr int kSlack = 64;                // a compaction keeps between budget and budget + kSlack keys
+static_assert(kMaxBudget + kSlack < kCompactAt, "a compaction must free room for the next round");
 constexpr int kThreads = 320;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
@@ -421,7 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int qq = 0; qq < 4; ++qq) {
                 const int b = __shfl_sync(0xffffffffu, base, qq);
-                if ((m[qq] >> lane) & 1u) s_cand[(4 * bq + qq) * kCap + b + __popc(m[qq] & lt_mask)] = key[qq];
+                const int slot = b + __popc(m[qq] & lt_mask);
+                if ((m[qq] >> lane) & 1u) {
+                  if (slot < kCap) s_cand[(4 * bq + qq) * kCap + slot] = key[qq];
+                  else record_error(hdr, KPOOL_ERR_INTERNAL);  // cannot happen: kCompactAt leaves room
+                }
               }
             }
           }

@@ -26,6 +26,7 @@ KPOOL_ERR_UNSUPPORTED = 2
 KPOOL_ERR_WORKSPACE = 3
 KPOOL_ERR_CUDA = 4
 KPOOL_ERR_DEVICE_TIMEOUT = 5
+KPOOL_ERR_INTERNAL = 6
 
 KPOOL_BF16 = 0
 KPOOL_F32 = 1

@@ -113,12 +113,30 @@ def test_integer_ragged_exact(kernel):
                   scale=1.0 / 16, dtype="bf16", values="integer", seed=43, dup_every=8)
     inp = W.generate(wl, "cpu")
     dev = to_dev(inp)
-    ids, toks, sc = run(dev, wl, score_kernel=kernel)
+    ws = K.new_workspace(wl.total_tokens, wl.num_seqs, 32, 128, K.KPOOL_BF16, 4, 2048)
+    ids, toks, sc = run(dev, wl, score_kernel=kernel, workspace=ws)
+    assert K.kpool_last_device_error(ws) == K.KPOOL_OK
     ref = full_oracle(inp, wl)
     parity.assert_exact(ref, ids, toks)
     m = ref["pool_ids"] >= 0
     np.testing.assert_array_equal(sc[m], ref["scores"][m].astype(np.float32))
     check_properties(dev, wl, ids, sc, toks)
+
+
+def test_integer_long_rows_exact():
+    """Rows with up to 3000 eligible pools: many compactions per row, still bit-exact."""
+    wl = W.custom("intlong", (12000, 333), heads=32, head_dim=128, kpool=4, index_topk=2048, scale=1.0 / 16,
+                  dtype="bf16", values="integer", seed=44, dup_every=8)
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    ids, toks, sc = run(dev, wl)
+    check_properties(dev, wl, ids, sc, toks)
+    rows = W.sample_rows(wl, 600).numpy()
+    ref = parity.oracle_rows(inp, wl, rows)
+    parity.assert_exact(ref, ids[rows], toks[rows])
+    ws_check = K.new_workspace(wl.total_tokens, wl.num_seqs, 32, 128, K.KPOOL_BF16, 4, 2048)
+    K.kpool_select_ex(dev["q"], dev["k"], dev["w"], dev["cu_seqlens"], 4, 2048, wl.scale, workspace=ws_check)
+    assert K.kpool_last_device_error(ws_check) == K.KPOOL_OK
 
 
 def test_tie_heavy_workload_exact():
