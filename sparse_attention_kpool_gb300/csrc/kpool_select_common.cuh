@@ -172,4 +172,177 @@ __device__ __forceinline__ void warp_sort_regs_desc(uint64_t (&k)[kSlots]) {
   }
 }
 
+// One register stage of warp_sort_regs_desc_rolled: pairs (r, r | RS) of the same lane.
+template <int RS, int kSlots>
+__device__ __forceinline__ void sort_reg_stage(uint64_t (&k)[kSlots], int size) {
+#pragma unroll
+  for (int r = 0; r < kSlots; ++r) {
+    if ((r & RS) == 0) {
+      const int r2 = r | RS;
+      const bool desc = ((32 * r) & size) == 0;
+      const uint64_t a = k[r], b = k[r2];
+      const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+      k[r] = desc ? hi : lo;
+      k[r2] = desc ? lo : hi;
+    }
+  }
+}
+
+// Same network as warp_sort_regs_desc for 512 keys (16 per lane), with the stage
+// loops kept rolled so the code stays small (it runs once per row and item).
+__device__ __forceinline__ void warp_sort512_regs_desc(uint64_t (&k)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int size = 2; size <= 512; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32) {
+        switch (stride >> 5) {
+          case 1: sort_reg_stage<1>(k, size); break;
+          case 2: sort_reg_stage<2>(k, size); break;
+          case 4: sort_reg_stage<4>(k, size); break;
+          default: sort_reg_stage<8>(k, size); break;
+        }
+      } else {
+        const bool lower = (lane & stride) == 0;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const uint64_t other = __shfl_xor_sync(0xffffffffu, k[r], stride);
+          const bool desc = ((32 * r + lane) & size) == 0;
+          const uint64_t hi = k[r] > other ? k[r] : other, lo = k[r] > other ? other : k[r];
+          k[r] = lower == desc ? hi : lo;
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void group_bar(int id, int count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Scratch (shared memory) of block_select_compact: per-warp OR/AND words, three
+// rotating 32-bin histograms and per-warp kept counts.
+struct SelectScratch {
+  unsigned long long red_or[8];
+  unsigned long long red_and[8];
+  uint32_t hist[3][32];
+  int32_t kept[8];
+};
+
+// Threshold search + compaction of one candidate buffer by the 8 warps (256
+// threads, barrier `bar_id`) that call it together. Same search as
+// warp_select_compact -- 5-bit most-significant-digit passes starting below the
+// keys' common leading bits -- with each thread holding 4 of the (at most 1024)
+// keys and the histograms shared, so a compaction costs a handful of barriers
+// instead of one warp's long dependent chain. Returns the kept count (between
+// budget and budget + slack, or all keys when n <= budget); *edge_out gets the
+// edge. Ends with a barrier: buf and the returned count are consistent for all.
+__device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int slack, int et, int bar_id,
+                                           SelectScratch* sc, uint64_t* edge_out) {
+  const int lane = et & 31, wid = et >> 5;
+  const unsigned full = 0xffffffffu;
+  uint64_t k[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int idx = et + 256 * j;
+    k[j] = idx < n ? buf[idx] : 0ull;
+  }
+  uint64_t o = 0, a = ~0ull;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (k[j] != 0) {
+      o |= k[j];
+      a &= k[j];
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    o |= __shfl_xor_sync(full, o, off);
+    a &= __shfl_xor_sync(full, a, off);
+  }
+  if (lane == 0) {
+    sc->red_or[wid] = o;
+    sc->red_and[wid] = a;
+  }
+  if (wid == 0) {
+    sc->hist[0][lane] = 0;
+    sc->hist[1][lane] = 0;
+  }
+  group_bar(bar_id, 256);
+  o = 0;
+  a = ~0ull;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    o |= sc->red_or[w];
+    a &= sc->red_and[w];
+  }
+  const uint64_t diff = o ^ a;
+  uint64_t edge = a;  // one distinct key (or none): keep it
+  if (n > budget && diff != 0) {
+    int pbits = __clzll(static_cast<long long>(diff));  // leading bits common to every key
+    uint64_t prefix = pbits == 0 ? 0ull : (a & ~(~0ull >> pbits));
+    int above = 0;
+    for (int pass = 0;; ++pass) {
+      uint32_t* hist = sc->hist[pass % 3];
+      const int width = (64 - pbits) < 5 ? (64 - pbits) : 5;
+      const int dshift = 64 - pbits - width;
+      const uint64_t dmask = (1ull << width) - 1ull;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool in = k[j] != 0 && (pbits == 0 || (k[j] >> (64 - pbits)) == (prefix >> (64 - pbits)));
+        if (in) atomicAdd(hist + int((k[j] >> dshift) & dmask), 1u);
+      }
+      group_bar(bar_id, 256);
+      if (wid == 0) sc->hist[(pass + 2) % 3][lane] = 0;  // read by every warp before this barrier
+      const int cnt = int(hist[lane]);
+      int suffix = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_down_sync(full, suffix, off);
+        if (lane + off < 32) suffix += v;
+      }
+      const int higher = suffix - cnt;
+      const unsigned hit = __ballot_sync(full, above + higher < budget && above + suffix >= budget);
+      const int d = hit ? __ffs(hit) - 1 : 0;  // a crossing bin always exists (above < budget <= bin total)
+      const int d_higher = __shfl_sync(full, higher, d);
+      const int d_cnt = __shfl_sync(full, cnt, d);
+      prefix |= uint64_t(d) << dshift;
+      pbits += width;
+      if (above + d_higher + d_cnt <= budget + slack || pbits == 64) {
+        edge = prefix;
+        break;
+      }
+      above += d_higher;
+    }
+  } else if (n <= budget) {
+    edge = 1;  // keep everything
+  }
+  // write the kept keys back to the front of buf, in thread order
+  unsigned m[4];
+  int mine = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    m[j] = __ballot_sync(full, k[j] != 0 && k[j] >= edge);
+    mine += __popc(m[j]);
+  }
+  if (lane == 0) sc->kept[wid] = mine;
+  group_bar(bar_id, 256);
+  int off = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int c = sc->kept[w];
+    off += w < wid ? c : 0;
+    total += c;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if ((m[j] >> lane) & 1u) buf[off + __popc(m[j] & lt)] = k[j];
+    off += __popc(m[j]);
+  }
+  *edge_out = edge;
+  group_bar(bar_id, 256);
+  return total;
+}
+
 }  // namespace kpool

@@ -34,11 +34,11 @@
 //               |scale|*w, head sum in fp32 (packed f32x2 FMAs) -> selection key
 //               -> threshold filter -> candidate buffer in shared memory.
 // Selection: 1024 candidate slots per query row. A key enters only if it beats
-// the row's threshold. When a buffer passes 768 entries its owning warp runs a
-// radix threshold search in registers and keeps between budget and budget+64
-// keys; the threshold rises to the search's edge. After the last tile the warp
-// cuts the buffer to exactly `budget` keys, sorts them in registers (bitonic)
-// and writes the ranked ids.
+// the row's threshold. When a buffer passes 768 entries all 8 epilogue warps run
+// a radix threshold search over it together and keep between budget and
+// budget+64 keys; the threshold rises to the search's edge. After the last tile
+// each row is cut to exactly `budget` keys the same way, then one warp per row
+// sorts them in registers (bitonic) and writes the ranked ids.
 //
 // Every mbarrier wait is bounded (poll count and ~1 s of wall time). A wait that
 // runs out records KPOOL_ERR_DEVICE_TIMEOUT in the workspace header; all roles
@@ -50,6 +50,10 @@
 #include "kpool_internal.cuh"
 #include "kpool_ptx.cuh"
 #include "kpool_select_common.cuh"
+
+#ifndef KPOOL_TC_BATCH_ROWS
+#define KPOOL_TC_BATCH_ROWS 2
+#endif
 
 namespace kpool {
 namespace {
@@ -66,6 +70,7 @@ constexpr int kMaxBudget = 512;
 // candidates per row, so a row is compacted once it holds more than kCap - 256.
 constexpr int kCompactAt = kCap - 2 * kTilePools;
 constexpr int kSlack = 64;                // a compaction keeps between budget and budget + kSlack keys
+constexpr int kBatchRows = KPOOL_TC_BATCH_ROWS;  // rows per TMEM load batch in the epilogue
 static_assert(kMaxBudget + kSlack < kCompactAt, "a compaction must free room for the next round");
 constexpr int kThreads = 320;
 constexpr int kAccCols = 256;
@@ -86,8 +91,8 @@ constexpr uint32_t kOffCount = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffTau = (kOffCount + kRows * 4 + 7) & ~7u;
 constexpr uint32_t kOffElig = kOffTau + kRows * 8;
 constexpr uint32_t kOffMisc = kOffElig + kRows * 4;
-constexpr uint32_t kOffHist = kOffMisc + 16;                // 16 words per epilogue warp
-constexpr uint32_t kSmemUsed = kOffHist + 8 * 16 * 4;
+constexpr uint32_t kOffSelect = kOffMisc + 16;              // SelectScratch
+constexpr uint32_t kSmemUsed = kOffSelect + ((sizeof(SelectScratch) + 15) & ~size_t(15));
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
@@ -183,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   int32_t* s_abort = reinterpret_cast<int32_t*>(smem + kOffMisc + 4);
   float* s_w = reinterpret_cast<float*>(smem + kOffW);
-  uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
+  SelectScratch* s_sel = reinterpret_cast<SelectScratch*>(smem + kOffSelect);
   uint64_t* s_cand = reinterpret_cast<uint64_t*>(smem + kOffCand);
 
   // n_items was written by the planning kernel before this launch and is 0 when
@@ -377,22 +382,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const int p = t * kTilePools + lg * 32 + lane;  // sequence-local pool index of this thread
 #pragma unroll
-            for (int bq = 0; bq < 2; ++bq) {  // rows 4bq .. 4bq+3
-              uint32_t v[4][32];
+            for (int bq = 0; bq < kRows / kBatchRows; ++bq) {  // rows kBatchRows*bq ..
+              uint32_t v[kBatchRows][32];
 #pragma unroll
-              for (int qq = 0; qq < 4; ++qq)
-                ptx::tc_ld_32x32b_x32(lane_addr + uint32_t((4 * bq + qq) * kHeads), v[qq]);
+              for (int qq = 0; qq < kBatchRows; ++qq)
+                ptx::tc_ld_32x32b_x32(lane_addr + uint32_t((kBatchRows * bq + qq) * kHeads), v[qq]);
               ptx::tc_wait_ld();
-              if (bq == 1) {  // every column is in registers: hand the accumulator back
+              if (bq == kRows / kBatchRows - 1) {  // every column is in registers: hand the accumulator back
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar.acc_empty + grp);
               }
-              uint64_t key[4];
-              unsigned m[4];
+              uint64_t key[kBatchRows];
+              unsigned m[kBatchRows];
 #pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
-                const int q = 4 * bq + qq;
+              for (int qq = 0; qq < kBatchRows; ++qq) {
+                const int q = kBatchRows * bq + qq;
                 const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + q * kHeads);
                 // heads 4i, 4i+1 accumulate in acc0 and 4i+2, 4i+3 in acc1 (four partial
                 // sums, two fp32 lanes each), added at the end
@@ -416,17 +421,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 key[qq] = p < s_elig[q] ? make_key(s, uint32_t(p)) : 0ull;
                 m[qq] = __ballot_sync(0xffffffffu, key[qq] > s_tau[q]);
               }
-              // lanes 0..3 reserve buffer slots for the four rows with one shared atomic
-              const unsigned my_m = lane == 0 ? m[0] : lane == 1 ? m[1] : lane == 2 ? m[2] : m[3];
-              int base = 0;
-              if (lane < 4 && my_m != 0) base = atomicAdd(s_count + 4 * bq + lane, __popc(my_m));
-              over = over || (lane < 4 && base + __popc(my_m) > kCompactAt);
+              // lanes 0..kBatchRows-1 reserve buffer slots for the batch's rows with one shared atomic
+              unsigned my_m = 0;
 #pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
+              for (int qq = 0; qq < kBatchRows; ++qq) my_m = lane == qq ? m[qq] : my_m;
+              int base = 0;
+              if (lane < kBatchRows && my_m != 0) base = atomicAdd(s_count + kBatchRows * bq + lane, __popc(my_m));
+              over = over || (lane < kBatchRows && base + __popc(my_m) > kCompactAt);
+#pragma unroll
+              for (int qq = 0; qq < kBatchRows; ++qq) {
                 const int b = __shfl_sync(0xffffffffu, base, qq);
                 const int slot = b + __popc(m[qq] & lt_mask);
                 if ((m[qq] >> lane) & 1u) {
-                  if (slot < kCap) s_cand[(4 * bq + qq) * kCap + slot] = key[qq];
+                  if (slot < kCap) s_cand[(kBatchRows * bq + qq) * kCap + slot] = key[qq];
                   else record_error(hdr, KPOOL_ERR_INTERNAL);  // cannot happen: kCompactAt leaves room
                 }
               }
@@ -440,38 +447,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             aborted = true;
             break;
           }
-          const int n = s_count[ew];  // warp ew brings row ew back below the compaction mark
-          if (n > kCompactAt) {
-            uint64_t edge;
-            const int kept = warp_select_compact<kCap / 32>(s_cand + ew * kCap, n, budget, kSlack,
-                                                            s_hist + ew * 16, &edge);
-            if (lane == 0) {
-              s_count[ew] = kept;
-              s_tau[ew] = edge - 1;  // a key must reach the edge to matter from now on
+          // all 8 warps bring each overfull row back below the compaction mark together
+          for (int q = 0; q < kRows; ++q) {
+            const int n = s_count[q];
+            if (n > kCompactAt) {
+              uint64_t edge;
+              const int kept = block_select_compact(s_cand + q * kCap, n, budget, kSlack, et, 1, s_sel, &edge);
+              if (et == 0) {
+                s_count[q] = kept;
+                s_tau[q] = edge - 1;  // a key must reach the edge to matter from now on
+              }
             }
           }
-          __syncwarp();
           named_bar(1, 256);
         }
       }
       if (aborted) break;
       g += uint32_t(it.n_tiles);
-      {  // final ranking of row ew
+      // final ranking: cut each row to its top `budget` (all 8 warps together), then
+      // warp ew sorts row ew in registers and writes it in rank order
+      for (int q = 0; q < kRows; ++q) {
+        const int n = s_count[q];
+        if (n > budget) {
+          uint64_t edge;
+          const int kept = block_select_compact(s_cand + q * kCap, n, budget, 0, et, 1, s_sel, &edge);
+          if (et == 0) s_count[q] = kept;
+        }
+      }
+      named_bar(1, 256);
+      {
         const int row = it.t0 + ew;
         if (row < it.len) {
-          uint64_t* buf = s_cand + ew * kCap;
-          int n = s_count[ew];
-          if (n > budget) {  // cut to exactly the top `budget` (slack 0), unordered
-            uint64_t edge;
-            n = warp_select_compact<kCap / 32>(buf, n, budget, 0, s_hist + ew * 16, &edge);
-          }
+          const uint64_t* buf = s_cand + ew * kCap;
+          const int n = s_count[ew];
           uint64_t kk[kMaxBudget / 32];
 #pragma unroll
           for (int j = 0; j < kMaxBudget / 32; ++j) {
             const int e = 32 * j + lane;
             kk[j] = e < n ? buf[e] : 0ull;
           }
-          warp_sort_regs_desc<kMaxBudget / 32>(kk);
+          warp_sort512_regs_desc(kk);
           const int64_t grow = it.seq_start + row;
 #pragma unroll
           for (int j = 0; j < kMaxBudget / 32; ++j) {
