@@ -163,6 +163,14 @@ __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[3
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// After tc_wait_ld: tells the compiler that the registers a tcgen05.ld filled
+// change here, so no use of them can be scheduled before the wait (the load
+// writes them asynchronously, which the asm outputs of the load cannot express).
+__device__ __forceinline__ void tc_reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // ------------------------------------------------------- packed fp32 pairs
 
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {

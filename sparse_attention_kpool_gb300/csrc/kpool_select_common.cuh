@@ -233,24 +233,25 @@ struct SelectScratch {
 // Threshold search + compaction of one candidate buffer by the 8 warps (256
 // threads, barrier `bar_id`) that call it together. Same search as
 // warp_select_compact -- 5-bit most-significant-digit passes starting below the
-// keys' common leading bits -- with each thread holding 4 of the (at most 1024)
-// keys and the histograms shared, so a compaction costs a handful of barriers
-// instead of one warp's long dependent chain. Returns the kept count (between
-// budget and budget + slack, or all keys when n <= budget); *edge_out gets the
-// edge. Ends with a barrier: buf and the returned count are consistent for all.
+// keys' common leading bits -- with each thread holding kPer of the (at most
+// 256 * kPer) keys and the histograms shared, so a compaction costs a handful of
+// barriers instead of one warp's long dependent chain. Returns the kept count
+// (between budget and budget + slack, or all keys when n <= budget); *edge_out
+// gets the edge. Ends with a barrier: buf and the count are consistent for all.
+template <int kPer>
 __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int slack, int et, int bar_id,
                                            SelectScratch* sc, uint64_t* edge_out) {
   const int lane = et & 31, wid = et >> 5;
   const unsigned full = 0xffffffffu;
-  uint64_t k[4];
+  uint64_t k[kPer];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < kPer; ++j) {
     const int idx = et + 256 * j;
     k[j] = idx < n ? buf[idx] : 0ull;
   }
   uint64_t o = 0, a = ~0ull;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int j = 0; j < kPer; ++j)
     if (k[j] != 0) {
       o |= k[j];
       a &= k[j];
@@ -288,7 +289,7 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
       const int dshift = 64 - pbits - width;
       const uint64_t dmask = (1ull << width) - 1ull;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kPer; ++j) {
         const bool in = k[j] != 0 && (pbits == 0 || (k[j] >> (64 - pbits)) == (prefix >> (64 - pbits)));
         if (in) atomicAdd(hist + int((k[j] >> dshift) & dmask), 1u);
       }
@@ -318,10 +319,10 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
     edge = 1;  // keep everything
   }
   // write the kept keys back to the front of buf, in thread order
-  unsigned m[4];
+  unsigned m[kPer];
   int mine = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < kPer; ++j) {
     m[j] = __ballot_sync(full, k[j] != 0 && k[j] >= edge);
     mine += __popc(m[j]);
   }
@@ -336,7 +337,7 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
   }
   const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < kPer; ++j) {
     if ((m[j] >> lane) & 1u) buf[off + __popc(m[j] & lt)] = k[j];
     off += __popc(m[j]);
   }

@@ -24,7 +24,8 @@
 //
 // Warp roles (10 warps, one CTA per SM, persistent):
 //   warp 0      TMA producer: the item's q tile (64 KB), then pool tiles into a
-//               3-stage ring (32 KB each).
+//               2-stage ring (32 KB each); a third stage measured no faster and
+//               its 32 KB buys 50% larger candidate buffers instead.
 //   warp 1      TMEM owner and MMA issuer: two 256-column accumulators, so the
 //               epilogue drains one while the tensor core fills the other.
 //   warps 2..9  epilogue, two groups of four warps in ping-pong: group g drains
@@ -33,8 +34,8 @@
 //               TMEM lanes 32*(w%4).. (the hardware rule). tcgen05.ld -> relu,
 //               |scale|*w, head sum in fp32 (packed f32x2 FMAs) -> selection key
 //               -> threshold filter -> candidate buffer in shared memory.
-// Selection: 1024 candidate slots per query row. A key enters only if it beats
-// the row's threshold. When a buffer passes 768 entries all 8 epilogue warps run
+// Selection: 1536 candidate slots per query row. A key enters only if it beats
+// the row's threshold. When a buffer passes 1280 entries all 8 epilogue warps run
 // a radix threshold search over it together and keep between budget and
 // budget+64 keys; the threshold rises to the search's edge. After the last tile
 // each row is cut to exactly `budget` keys the same way, then one warp per row
@@ -51,10 +52,6 @@
 #include "kpool_ptx.cuh"
 #include "kpool_select_common.cuh"
 
-#ifndef KPOOL_TC_BATCH_ROWS
-#define KPOOL_TC_BATCH_ROWS 2
-#endif
-
 namespace kpool {
 namespace {
 
@@ -63,14 +60,23 @@ constexpr int kDim = 128;
 constexpr int kRows = kItemRows;          // query rows per item
 constexpr int kN = kRows * kHeads;        // 256 MMA columns
 constexpr int kTilePools = 128;           // MMA M
-constexpr int kStages = 3;
-constexpr int kCap = 1024;                // candidate slots per query row
+#ifndef KPOOL_TC_STAGES
+#define KPOOL_TC_STAGES 2
+#endif
+#ifndef KPOOL_TC_CAP
+#define KPOOL_TC_CAP 1536
+#endif
+#ifndef KPOOL_TC_SLACK
+#define KPOOL_TC_SLACK 64
+#endif
+constexpr int kStages = KPOOL_TC_STAGES;  // pool-tile ring depth
+constexpr int kCap = KPOOL_TC_CAP;        // candidate slots per query row
 constexpr int kMaxBudget = 512;
 // A barrier round covers two tiles (one per epilogue group), i.e. up to 256 new
 // candidates per row, so a row is compacted once it holds more than kCap - 256.
 constexpr int kCompactAt = kCap - 2 * kTilePools;
-constexpr int kSlack = 64;                // a compaction keeps between budget and budget + kSlack keys
-constexpr int kBatchRows = KPOOL_TC_BATCH_ROWS;  // rows per TMEM load batch in the epilogue
+static_assert(kCap % 256 == 0, "the cooperative compaction gives each of 256 threads kCap/256 keys");
+constexpr int kSlack = KPOOL_TC_SLACK;    // a compaction keeps between budget and budget + kSlack keys
 static_assert(kMaxBudget + kSlack < kCompactAt, "a compaction must free room for the next round");
 constexpr int kThreads = 320;
 constexpr int kAccCols = 256;
@@ -381,23 +387,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1;
             ptx::tc_fence_after();
             const int p = t * kTilePools + lg * 32 + lane;  // sequence-local pool index of this thread
+            // TMEM -> registers two rows at a time, software-pipelined: the load of the
+            // next pair is in flight while the current pair is scored. Candidate slots
+            // are reserved once per four rows.
+            uint32_t va[2][32], vb[2][32];
+            uint64_t key[4];
+            unsigned m[4];
+            ptx::tc_ld_32x32b_x32(lane_addr + 0 * kHeads, va[0]);
+            ptx::tc_ld_32x32b_x32(lane_addr + 1 * kHeads, va[1]);
+            ptx::tc_wait_ld();
+            ptx::tc_reg_fence(va[0]);
+            ptx::tc_reg_fence(va[1]);
 #pragma unroll
-            for (int bq = 0; bq < kRows / kBatchRows; ++bq) {  // rows kBatchRows*bq ..
-              uint32_t v[kBatchRows][32];
-#pragma unroll
-              for (int qq = 0; qq < kBatchRows; ++qq)
-                ptx::tc_ld_32x32b_x32(lane_addr + uint32_t((kBatchRows * bq + qq) * kHeads), v[qq]);
-              ptx::tc_wait_ld();
-              if (bq == kRows / kBatchRows - 1) {  // every column is in registers: hand the accumulator back
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar.acc_empty + grp);
+            for (int pair = 0; pair < kRows / 2; ++pair) {
+              uint32_t (&cur)[2][32] = (pair & 1) ? vb : va;
+              uint32_t (&nxt)[2][32] = (pair & 1) ? va : vb;
+              if (pair + 1 < kRows / 2) {
+                ptx::tc_ld_32x32b_x32(lane_addr + uint32_t((2 * pair + 2) * kHeads), nxt[0]);
+                ptx::tc_ld_32x32b_x32(lane_addr + uint32_t((2 * pair + 3) * kHeads), nxt[1]);
               }
-              uint64_t key[kBatchRows];
-              unsigned m[kBatchRows];
 #pragma unroll
-              for (int qq = 0; qq < kBatchRows; ++qq) {
-                const int q = kBatchRows * bq + qq;
+              for (int qq = 0; qq < 2; ++qq) {
+                const int q = 2 * pair + qq;
                 const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + q * kHeads);
                 // heads 4i, 4i+1 accumulate in acc0 and 4i+2, 4i+3 in acc1 (four partial
                 // sums, two fp32 lanes each), added at the end
@@ -405,10 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h4 = 0; h4 < kHeads / 4; ++h4) {
                   const ulonglong2 ww = wv[h4];
-                  const float x0 = __uint_as_float(v[qq][4 * h4 + 0]);
-                  const float x1 = __uint_as_float(v[qq][4 * h4 + 1]);
-                  const float x2 = __uint_as_float(v[qq][4 * h4 + 2]);
-                  const float x3 = __uint_as_float(v[qq][4 * h4 + 3]);
+                  const float x0 = __uint_as_float(cur[qq][4 * h4 + 0]);
+                  const float x1 = __uint_as_float(cur[qq][4 * h4 + 1]);
+                  const float x2 = __uint_as_float(cur[qq][4 * h4 + 2]);
+                  const float x3 = __uint_as_float(cur[qq][4 * h4 + 3]);
                   acc0 = ptx::fma_f32x2(ww.x, ptx::pack_f32x2(fmaxf(kNegScale ? -x0 : x0, 0.0f),
                                                               fmaxf(kNegScale ? -x1 : x1, 0.0f)), acc0);
                   acc1 = ptx::fma_f32x2(ww.y, ptx::pack_f32x2(fmaxf(kNegScale ? -x2 : x2, 0.0f),
@@ -418,23 +429,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::unpack_f32x2(acc0, s0, s1);
                 ptx::unpack_f32x2(acc1, s2, s3);
                 const float s = (s0 + s1) + (s2 + s3);
-                key[qq] = p < s_elig[q] ? make_key(s, uint32_t(p)) : 0ull;
-                m[qq] = __ballot_sync(0xffffffffu, key[qq] > s_tau[q]);
+                key[q & 3] = p < s_elig[q] ? make_key(s, uint32_t(p)) : 0ull;
+                m[q & 3] = __ballot_sync(0xffffffffu, key[q & 3] > s_tau[q]);
               }
-              // lanes 0..kBatchRows-1 reserve buffer slots for the batch's rows with one shared atomic
-              unsigned my_m = 0;
+              if (pair + 1 < kRows / 2) {
+                ptx::tc_wait_ld();
+                ptx::tc_reg_fence(nxt[0]);
+                ptx::tc_reg_fence(nxt[1]);
+              }
+              if (pair + 1 == kRows / 2 - 1) {  // the last pair is in registers: hand the accumulator back
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar.acc_empty + grp);
+              }
+              if (pair & 1) {  // rows 4h .. 4h+3 scored: lanes 0..3 reserve their slots with one atomic
+                const int r0 = 2 * pair - 2;
+                unsigned my_m = 0;
 #pragma unroll
-              for (int qq = 0; qq < kBatchRows; ++qq) my_m = lane == qq ? m[qq] : my_m;
-              int base = 0;
-              if (lane < kBatchRows && my_m != 0) base = atomicAdd(s_count + kBatchRows * bq + lane, __popc(my_m));
-              over = over || (lane < kBatchRows && base + __popc(my_m) > kCompactAt);
+                for (int qq = 0; qq < 4; ++qq) my_m = lane == qq ? m[qq] : my_m;
+                int base = 0;
+                if (lane < 4 && my_m != 0) base = atomicAdd(s_count + r0 + lane, __popc(my_m));
+                over = over || (lane < 4 && base + __popc(my_m) > kCompactAt);
 #pragma unroll
-              for (int qq = 0; qq < kBatchRows; ++qq) {
-                const int b = __shfl_sync(0xffffffffu, base, qq);
-                const int slot = b + __popc(m[qq] & lt_mask);
-                if ((m[qq] >> lane) & 1u) {
-                  if (slot < kCap) s_cand[(kBatchRows * bq + qq) * kCap + slot] = key[qq];
-                  else record_error(hdr, KPOOL_ERR_INTERNAL);  // cannot happen: kCompactAt leaves room
+                for (int qq = 0; qq < 4; ++qq) {
+                  const int b = __shfl_sync(0xffffffffu, base, qq);
+                  const int slot = b + __popc(m[qq] & lt_mask);
+                  if ((m[qq] >> lane) & 1u) {
+                    if (slot < kCap) s_cand[(r0 + qq) * kCap + slot] = key[qq];
+                    else record_error(hdr, KPOOL_ERR_INTERNAL);  // cannot happen: kCompactAt leaves room
+                  }
                 }
               }
             }
@@ -452,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = s_count[q];
             if (n > kCompactAt) {
               uint64_t edge;
-              const int kept = block_select_compact(s_cand + q * kCap, n, budget, kSlack, et, 1, s_sel, &edge);
+              const int kept = block_select_compact<kCap / 256>(s_cand + q * kCap, n, budget, kSlack, et, 1, s_sel, &edge);
               if (et == 0) {
                 s_count[q] = kept;
                 s_tau[q] = edge - 1;  // a key must reach the edge to matter from now on
@@ -470,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = s_count[q];
         if (n > budget) {
           uint64_t edge;
-          const int kept = block_select_compact(s_cand + q * kCap, n, budget, 0, et, 1, s_sel, &edge);
+          const int kept = block_select_compact<kCap / 256>(s_cand + q * kCap, n, budget, 0, et, 1, s_sel, &edge);
           if (et == 0) s_count[q] = kept;
         }
       }
