@@ -38,11 +38,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
+// One poll; the hardware may suspend the thread for up to ~1 ms (suspend-time
+// hint) while the phase is incomplete and wakes it when the phase completes.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
@@ -58,12 +60,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Waits for the phase of `bar` with the given parity to complete. Gives up
 // (returns false) after `max_polls` polls or `max_ns` nanoseconds of wall
-// time, whichever comes first, so no wait can hang the GPU.
+// time, whichever comes first, so no wait can hang the GPU. A thread off the
+// critical path passes sleep_ns > 0 to back off between polls (__nanosleep),
+// leaving the issue slots of its SM sub-partition to the warps that compute.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int64_t max_polls,
-                                                  uint64_t max_ns) {
+                                                  uint64_t max_ns, uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (int64_t i = 1; i < max_polls; ++i) {
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255) == 0 && globaltimer_ns() - t0 > max_ns) return false;
   }

@@ -102,7 +102,11 @@ constexpr uint32_t kSmemUsed = kOffSelect + ((sizeof(SelectScratch) + 15) & ~siz
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
+#ifndef KPOOL_TC_BACKOFF_NS
+#define KPOOL_TC_BACKOFF_NS 0
+#endif
 constexpr int64_t kMaxPolls = int64_t(1) << 40;
+constexpr uint32_t kBackoffNs = KPOOL_TC_BACKOFF_NS;  // producer / MMA poll back-off
 constexpr uint64_t kMaxWaitNs = 1000000000ull;  // 1 s; legitimate waits are microseconds
 
 struct Bars {
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx >= n_items) break;
         const Item it = load_item(items, cu, pool_off, idx, kpool);
         if (it.n_tiles == 0) continue;
-        if (!ptx::mbar_wait_bounded(bar.q_empty, q_phase ^ 1, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+        if (!ptx::mbar_wait_bounded(bar.q_empty, q_phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
           ok = false;
           break;
         }
@@ -256,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_2d_hint(qdst + kQHalfBytes, &tmap_q, bar.q_full, 64, qrow, pol_q);
         ++q_armed;
         for (int i = 0; i < it.n_tiles; ++i) {
-          if (!ptx::mbar_wait_bounded(bar.empty + stage, phase ^ 1, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+          if (!ptx::mbar_wait_bounded(bar.empty + stage, phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) ||
+              *abort_flag) {
             ok = false;
             break;
           }
@@ -297,15 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx >= n_items) break;
         const Item it = load_item(items, cu, pool_off, idx, kpool);
         if (it.n_tiles == 0) continue;
-        if (!ptx::mbar_wait_bounded(bar.q_full, q_phase, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+        if (!ptx::mbar_wait_bounded(bar.q_full, q_phase, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
           ok = false;
           break;
         }
         q_phase ^= 1;
         ptx::tc_fence_after();
         for (int i = 0; i < it.n_tiles; ++i) {
-          if (!ptx::mbar_wait_bounded(bar.acc_empty + acc, acc_phase ^ 1, kMaxPolls, kMaxWaitNs) ||
-              !ptx::mbar_wait_bounded(bar.full + stage, phase, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+          if (!ptx::mbar_wait_bounded(bar.acc_empty + acc, acc_phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) ||
+              !ptx::mbar_wait_bounded(bar.full + stage, phase, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
             ok = false;
             break;
           }
