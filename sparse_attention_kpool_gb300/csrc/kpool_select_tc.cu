@@ -99,7 +99,7 @@ constexpr uint32_t kOffElig = kOffTau + kRows * 8;
 constexpr uint32_t kOffMisc = kOffElig + kRows * 4;
 constexpr uint32_t kOffSelect = kOffMisc + 16;              // SelectScratch
 constexpr uint32_t kSmemUsed = kOffSelect + ((sizeof(SelectScratch) + 15) & ~size_t(15));
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+constexpr uint32_t kSmemBytes = kSmemUsed;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
 #ifndef KPOOL_TC_BACKOFF_NS
@@ -187,8 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const int32_t* __restrict__ pool_off, const int2* __restrict__ items,
                      WorkspaceHeader* __restrict__ hdr, int kpool, int budget, float abs_scale,
                      int32_t* __restrict__ out_ids, float* __restrict__ out_scores) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Pointers derived directly from the __shared__ array keep the shared address
+  // space, so the compiler emits shared loads, stores and atomics (LDS/STS/ATOMS)
+  // rather than generic ones.
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Bars bar = bars_at(smem);
@@ -201,6 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   SelectScratch* s_sel = reinterpret_cast<SelectScratch*>(smem + kOffSelect);
   uint64_t* s_cand = reinterpret_cast<uint64_t*>(smem + kOffCand);
 
+  // The 128-byte-swizzled TMA tiles need a 1024-byte aligned base. Every thread
+  // sees the same address, so this early exit is uniform (before any barrier).
+  if ((ptx::smem_addr(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(hdr, KPOOL_ERR_INTERNAL);
+    return;
+  }
   // n_items was written by the planning kernel before this launch and is 0 when
   // planning failed, so every thread reads the same value and the loops below
   // agree on how many items there are.
