@@ -54,15 +54,19 @@ inline WorkspaceLayout workspace_layout(int64_t T, int32_t S, int32_t d, size_t 
 // ------------------------------------------------------------ selection key
 //
 // A 64-bit key whose unsigned order is the selection order: the high word is
-// the score mapped to an order-preserving unsigned integer, the low word is
+// the score mapped to an order-preserving unsigned integer (sign bit set for
+// non-negative scores, all bits flipped for negative ones), the low word is
 // the bitwise complement of the pool index (so a smaller index ranks higher on
 // equal scores). -0 is folded into +0 first, so the two zeros tie. Finite
 // scores never produce the key 0, which therefore marks an empty slot.
+__device__ __forceinline__ uint32_t score_order_bits(float s) {
+  // x + 0.0f turns -0 into +0 (round to nearest) and leaves every other value as is
+  const uint32_t u = __float_as_uint(__fadd_rn(s, 0.0f));
+  return u ^ (uint32_t(int32_t(u) >> 31) | 0x80000000u);
+}
+
 __device__ __forceinline__ uint64_t make_key(float s, uint32_t pool) {
-  s = (s == 0.0f) ? 0.0f : s;
-  uint32_t u = __float_as_uint(s);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (uint64_t(u) << 32) | uint64_t(~pool);
+  return (uint64_t(score_order_bits(s)) << 32) | uint64_t(~pool);
 }
 
 __device__ __forceinline__ uint32_t key_pool(uint64_t key) { return ~uint32_t(key); }

@@ -442,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::unpack_f32x2(acc0, s0, s1);
                 ptx::unpack_f32x2(acc1, s2, s3);
                 const float s = (s0 + s1) + (s2 + s3);
-                key[q & 3] = p < s_elig[q] ? make_key(s, uint32_t(p)) : 0ull;
-                m[q & 3] = __ballot_sync(0xffffffffu, key[q & 3] > s_tau[q]);
+                key[q & 3] = make_key(s, uint32_t(p));
+                m[q & 3] = __ballot_sync(0xffffffffu, p < s_elig[q] && key[q & 3] > s_tau[q]);
               }
               if (pair + 1 < kRows / 2) {
                 ptx::tc_wait_ld();
@@ -461,16 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) my_m = lane == qq ? m[qq] : my_m;
                 int base = 0;
-                if (lane < 4 && my_m != 0) base = atomicAdd(s_count + r0 + lane, __popc(my_m));
+                if (lane < 4) base = atomicAdd(s_count + r0 + lane, __popc(my_m));
                 over = over || (lane < 4 && base + __popc(my_m) > kCompactAt);
+                // cannot happen (kCompactAt leaves room for a round); the stores below skip it
+                if (lane < 4 && base + __popc(my_m) > kCap) record_error(hdr, KPOOL_ERR_INTERNAL);
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
-                  const int b = __shfl_sync(0xffffffffu, base, qq);
-                  const int slot = b + __popc(m[qq] & lt_mask);
-                  if ((m[qq] >> lane) & 1u) {
-                    if (slot < kCap) s_cand[(r0 + qq) * kCap + slot] = key[qq];
-                    else record_error(hdr, KPOOL_ERR_INTERNAL);  // cannot happen: kCompactAt leaves room
-                  }
+                  const int slot = __shfl_sync(0xffffffffu, base, qq) + __popc(m[qq] & lt_mask);
+                  if (((m[qq] >> lane) & 1u) && slot < kCap) s_cand[(r0 + qq) * kCap + slot] = key[qq];
                 }
               }
             }
@@ -522,15 +520,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int e = 32 * j + lane;
             kk[j] = e < n ? buf[e] : 0ull;
           }
-          warp_sort512_regs_desc(kk);
+          warp_sort512_blocked_desc(kk);  // lane l now holds ranks 16 l .. 16 l + 15
           const int64_t grow = it.seq_start + row;
+          const int o0 = 16 * lane;
+          int32_t* dst_row = out_ids + grow * budget + o0;
+          if (o0 + 16 <= budget && (reinterpret_cast<uintptr_t>(dst_row) & 15u) == 0) {  // 16-byte vector stores
+            int4* dst = reinterpret_cast<int4*>(dst_row);
 #pragma unroll
-          for (int j = 0; j < kMaxBudget / 32; ++j) {
-            const int o = 32 * j + lane;
-            if (o < budget) {
-              out_ids[grow * budget + o] = kk[j] ? int32_t(key_pool(kk[j])) : -1;
-              if (out_scores) out_scores[grow * budget + o] = kk[j] ? key_score(kk[j]) : -INFINITY;
+            for (int j = 0; j < 4; ++j) {
+              int4 v;
+              v.x = kk[4 * j + 0] ? int32_t(key_pool(kk[4 * j + 0])) : -1;
+              v.y = kk[4 * j + 1] ? int32_t(key_pool(kk[4 * j + 1])) : -1;
+              v.z = kk[4 * j + 2] ? int32_t(key_pool(kk[4 * j + 2])) : -1;
+              v.w = kk[4 * j + 3] ? int32_t(key_pool(kk[4 * j + 3])) : -1;
+              dst[j] = v;
             }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (o0 + j < budget) out_ids[grow * budget + o0 + j] = kk[j] ? int32_t(key_pool(kk[j])) : -1;
+          }
+          if (out_scores) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (o0 + j < budget) out_scores[grow * budget + o0 + j] = kk[j] ? key_score(kk[j]) : -INFINITY;
           }
           __syncwarp();
         }
