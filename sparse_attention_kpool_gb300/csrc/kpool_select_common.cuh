@@ -278,23 +278,25 @@ struct SelectScratch {
   int32_t kept[8];
 };
 
-// Threshold search + compaction of one candidate buffer by the 8 warps (256
-// threads, barrier `bar_id`) that call it together. Same search as
+// Threshold search + compaction of one candidate buffer by the kWarps warps
+// (barrier `bar_id`) that call it together. Same search as
 // warp_select_compact -- 5-bit most-significant-digit passes starting below the
 // keys' common leading bits -- with each thread holding kPer of the (at most
-// 256 * kPer) keys and the histograms shared, so a compaction costs a handful of
+// 32 * kWarps * kPer) keys and the histograms shared, so a compaction costs a handful of
 // barriers instead of one warp's long dependent chain. Returns the kept count
 // (between budget and budget + slack, or all keys when n <= budget); *edge_out
 // gets the edge. Ends with a barrier: buf and the count are consistent for all.
-template <int kPer>
+template <int kPer, int kWarps>
 __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int slack, int et, int bar_id,
                                            SelectScratch* sc, uint64_t* edge_out) {
+  static_assert(kWarps <= 8, "SelectScratch holds 8 warps");
+  constexpr int kT = 32 * kWarps;
   const int lane = et & 31, wid = et >> 5;
   const unsigned full = 0xffffffffu;
   uint64_t k[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
-    const int idx = et + 256 * j;
+    const int idx = et + kT * j;
     k[j] = idx < n ? buf[idx] : 0ull;
   }
   uint64_t o = 0, a = ~0ull;
@@ -317,11 +319,11 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
     sc->hist[0][lane] = 0;
     sc->hist[1][lane] = 0;
   }
-  group_bar(bar_id, 256);
+  group_bar(bar_id, kT);
   o = 0;
   a = ~0ull;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < kWarps; ++w) {
     o |= sc->red_or[w];
     a &= sc->red_and[w];
   }
@@ -341,7 +343,7 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
         const bool in = k[j] != 0 && (pbits == 0 || (k[j] >> (64 - pbits)) == (prefix >> (64 - pbits)));
         if (in) atomicAdd(hist + int((k[j] >> dshift) & dmask), 1u);
       }
-      group_bar(bar_id, 256);
+      group_bar(bar_id, kT);
       if (wid == 0) sc->hist[(pass + 2) % 3][lane] = 0;  // read by every warp before this barrier
       const int cnt = int(hist[lane]);
       int suffix = cnt;
@@ -375,10 +377,10 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
     mine += __popc(m[j]);
   }
   if (lane == 0) sc->kept[wid] = mine;
-  group_bar(bar_id, 256);
+  group_bar(bar_id, kT);
   int off = 0, total = 0;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < kWarps; ++w) {
     const int c = sc->kept[w];
     off += w < wid ? c : 0;
     total += c;
@@ -390,7 +392,7 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
     off += __popc(m[j]);
   }
   *edge_out = edge;
-  group_bar(bar_id, 256);
+  group_bar(bar_id, kT);
   return total;
 }
 

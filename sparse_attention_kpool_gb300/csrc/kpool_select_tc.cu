@@ -28,15 +28,15 @@
 //               its 32 KB buys 50% larger candidate buffers instead.
 //   warp 1      TMEM owner and MMA issuer: two 256-column accumulators, so the
 //               epilogue drains one while the tensor core fills the other.
-//   warps 2..9  epilogue, two groups of four warps in ping-pong: group g drains
-//               accumulator g (every other tile) for all 8 rows, so one group's
-//               TMEM/atomic latency overlaps the other's arithmetic; warp w reads
-//               TMEM lanes 32*(w%4).. (the hardware rule). tcgen05.ld -> relu,
+//   warps 2..9  epilogue, two groups of four warps; group g owns rows 4g..4g+3
+//               of every item and reads their 128 columns of every accumulator;
+//               warp w reads TMEM lanes 32*(w%4).. (the hardware rule). The
+//               groups synchronise only within themselves. tcgen05.ld -> relu,
 //               |scale|*w, head sum in fp32 (packed f32x2 FMAs) -> selection key
 //               -> threshold filter -> candidate buffer in shared memory.
 // Selection: 1536 candidate slots per query row. A key enters only if it beats
-// the row's threshold. When a buffer passes 1280 entries all 8 epilogue warps run
-// a radix threshold search over it together and keep between budget and
+// the row's threshold. When a buffer passes 1408 entries the owning group's four
+// warps run a radix threshold search over it together and keep between budget and
 // budget+64 keys; the threshold rises to the search's edge. After the last tile
 // each row is cut to exactly `budget` keys the same way, then one warp per row
 // sorts them in registers (bitonic) and writes the ranked ids.
@@ -72,10 +72,10 @@ constexpr int kTilePools = 128;           // MMA M
 constexpr int kStages = KPOOL_TC_STAGES;  // pool-tile ring depth
 constexpr int kCap = KPOOL_TC_CAP;        // candidate slots per query row
 constexpr int kMaxBudget = 512;
-// A barrier round covers two tiles (one per epilogue group), i.e. up to 256 new
-// candidates per row, so a row is compacted once it holds more than kCap - 256.
-constexpr int kCompactAt = kCap - 2 * kTilePools;
-static_assert(kCap % 256 == 0, "the cooperative compaction gives each of 256 threads kCap/256 keys");
+// A tile adds at most one candidate per pool to a row (128), so a row is
+// compacted once it holds more than kCap - 128 after a tile.
+constexpr int kCompactAt = kCap - kTilePools;
+static_assert(kCap % 128 == 0, "a group's cooperative compaction gives each of 128 threads kCap/128 keys");
 constexpr int kSlack = KPOOL_TC_SLACK;    // a compaction keeps between budget and budget + kSlack keys
 static_assert(kMaxBudget + kSlack < kCompactAt, "a compaction must free room for the next round");
 constexpr int kThreads = 320;
@@ -98,7 +98,8 @@ constexpr uint32_t kOffTau = (kOffCount + kRows * 4 + 7) & ~7u;
 constexpr uint32_t kOffElig = kOffTau + kRows * 8;
 constexpr uint32_t kOffMisc = kOffElig + kRows * 4;
 constexpr uint32_t kOffSelect = kOffMisc + 16;              // SelectScratch
-constexpr uint32_t kSmemUsed = kOffSelect + ((sizeof(SelectScratch) + 15) & ~size_t(15));
+constexpr uint32_t kSelectBytes = (sizeof(SelectScratch) + 15) & ~size_t(15);
+constexpr uint32_t kSmemUsed = kOffSelect + 2 * kSelectBytes;  // one SelectScratch per epilogue group
 constexpr uint32_t kSmemBytes = kSmemUsed;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(bar.acc_full + a, 1);
-      ptx::mbar_init(bar.acc_empty + a, 4);
+      ptx::mbar_init(bar.acc_empty + a, 8);
     }
     ptx::mbar_init(bar.mma_done, 1);
     ptx::fence_mbar_init();
@@ -354,166 +355,167 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Ping-pong: group `grp` (warps 2-5 -> 0, warps 6-9 -> 1) drains accumulator grp,
-    // i.e. every other tile of the CTA's global tile sequence, for all 8 rows of the
-    // item; while one group waits on TMEM or on its atomics the other computes.
-    const int ew = warp - 2;          // 0..7, also the item row this warp ranks and compacts
-    const int grp = ew >> 2;          // accumulator this group drains
+    // Row split: group grp (warps 2-5 -> 0, warps 6-9 -> 1) owns rows 4*grp .. 4*grp+3
+    // of every item and reads those 128 columns of every accumulator. The groups share
+    // only the accumulators (each released once all 8 warps have loaded it), so each
+    // group synchronises just its own four warps and neither waits for the other's
+    // compactions.
+    const int ew = warp - 2;          // 0..7
+    const int grp = ew >> 2;          // 0 or 1
+    const int wq = ew & 3;            // row (within the group) this warp ranks at the end
     const int lg = warp & 3;          // TMEM lane group this warp may read
-    const int et = ew * 32 + lane;    // thread index among the 256 epilogue threads
+    const int gt = wq * 32 + lane;    // thread index within the group (0..127)
+    const int rbase = 4 * grp;        // the group's first row
+    const int bar_id = 1 + grp;
+    SelectScratch* sel = reinterpret_cast<SelectScratch*>(smem + kOffSelect + grp * kSelectBytes);
     const unsigned lt_mask = (1u << lane) - 1u;
-    const uint32_t lane_addr = tmem_base + (uint32_t(lg * 32) << 16) + uint32_t(grp * kAccCols);
-    uint32_t phase = 0;               // next phase of acc_full[grp] this group consumes
-    uint32_t g = 0;                   // tiles of this CTA before the current item
+    const uint32_t lane_addr = tmem_base + (uint32_t(lg * 32) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
     for (int r = 0;; ++r) {
       const int idx = item_index(r, blockIdx.x, gridDim.x);
       if (idx >= n_items) break;
       const Item it = load_item(items, cu, pool_off, idx, kpool);
-      // per-item state of the 8 rows
-      for (int e = et; e < kRows * kHeads; e += 256) {
-        const int q = e / kHeads, h = e % kHeads;
+      // per-item state of the group's 4 rows
+      {
+        const int q = rbase + (gt >> 5), h = gt & 31;
         const int row = it.t0 + q;
-        s_w[e] = row < it.len ? w[(it.seq_start + row) * kHeads + h] * abs_scale : 0.0f;
+        s_w[q * kHeads + h] = row < it.len ? w[(it.seq_start + row) * kHeads + h] * abs_scale : 0.0f;
       }
-      if (et < kRows) {
-        const int row = it.t0 + et;
-        s_count[et] = 0;
-        s_tau[et] = 0;
-        s_elig[et] = row < it.len ? (row + 1) / kpool : 0;
+      if (gt < 4) {
+        const int q = rbase + gt;
+        const int row = it.t0 + q;
+        s_count[q] = 0;
+        s_tau[q] = 0;
+        s_elig[q] = row < it.len ? (row + 1) / kpool : 0;
       }
-      named_bar(1, 256);
+      named_bar(bar_id, 128);
       bool aborted = false;
-      // round k pairs local tile 2k - (g&1) (group 0) with 2k - (g&1) + 1 (group 1)
-      const int n_rounds = it.n_tiles > 0 ? ((int(g & 1) + it.n_tiles - 1) >> 1) + 1 : 0;
-      for (int k = 0; k < n_rounds; ++k) {
-        const int t = 2 * k - int(g & 1) + grp;  // this group's local tile in the round
-        const bool has = t >= 0 && t < it.n_tiles;
+      for (int i = 0; i < it.n_tiles; ++i) {
         bool ready = true;
-        bool over = false;  // a reservation of this warp pushed a row past the compaction mark
-        if (has) {
-          if (lane == 0) ready = ptx::mbar_wait_bounded(bar.acc_full + grp, phase, kMaxPolls, kMaxWaitNs);
-          ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-          if (!ready) {
-            record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
-            *abort_flag = 1;
-          } else {
-            phase ^= 1;
-            ptx::tc_fence_after();
-            const int p = t * kTilePools + lg * 32 + lane;  // sequence-local pool index of this thread
-            // TMEM -> registers two rows at a time, software-pipelined: the load of the
-            // next pair is in flight while the current pair is scored. Candidate slots
-            // are reserved once per four rows.
-            uint32_t va[2][32], vb[2][32];
-            uint64_t key[4];
-            unsigned m[4];
-            ptx::tc_ld_32x32b_x32(lane_addr + 0 * kHeads, va[0]);
-            ptx::tc_ld_32x32b_x32(lane_addr + 1 * kHeads, va[1]);
-            ptx::tc_wait_ld();
-            ptx::tc_reg_fence(va[0]);
-            ptx::tc_reg_fence(va[1]);
+        bool over = false;  // this warp's reservation pushed a row past the compaction mark
+        if (lane == 0) ready = ptx::mbar_wait_bounded(bar.acc_full + acc, acc_phase, kMaxPolls, kMaxWaitNs);
+        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+        if (!ready) {
+          record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+          *abort_flag = 1;
+        } else {
+          ptx::tc_fence_after();
+          const int p = i * kTilePools + lg * 32 + lane;  // sequence-local pool index of this thread
+          const uint32_t col0 = lane_addr + uint32_t(acc * kAccCols + rbase * kHeads);
+          // TMEM -> registers two rows at a time; the second pair is in flight while
+          // the first is scored.
+          uint32_t va[2][32], vb[2][32];
+          uint64_t key[4];
+          unsigned m[4];
+          ptx::tc_ld_32x32b_x32(col0 + 0 * kHeads, va[0]);
+          ptx::tc_ld_32x32b_x32(col0 + 1 * kHeads, va[1]);
+          ptx::tc_wait_ld();
+          ptx::tc_reg_fence(va[0]);
+          ptx::tc_reg_fence(va[1]);
+          ptx::tc_ld_32x32b_x32(col0 + 2 * kHeads, vb[0]);
+          ptx::tc_ld_32x32b_x32(col0 + 3 * kHeads, vb[1]);
 #pragma unroll
-            for (int pair = 0; pair < kRows / 2; ++pair) {
-              uint32_t (&cur)[2][32] = (pair & 1) ? vb : va;
-              uint32_t (&nxt)[2][32] = (pair & 1) ? va : vb;
-              if (pair + 1 < kRows / 2) {
-                ptx::tc_ld_32x32b_x32(lane_addr + uint32_t((2 * pair + 2) * kHeads), nxt[0]);
-                ptx::tc_ld_32x32b_x32(lane_addr + uint32_t((2 * pair + 3) * kHeads), nxt[1]);
-              }
+          for (int pair = 0; pair < 2; ++pair) {
+            uint32_t (&cur)[2][32] = pair ? vb : va;
+            if (pair == 1) {
+              ptx::tc_wait_ld();
+              ptx::tc_reg_fence(vb[0]);
+              ptx::tc_reg_fence(vb[1]);
+              // every column this warp needs is in registers: release the accumulator
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(bar.acc_empty + acc);
+            }
 #pragma unroll
-              for (int qq = 0; qq < 2; ++qq) {
-                const int q = 2 * pair + qq;
-                const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + q * kHeads);
-                // heads 4i, 4i+1 accumulate in acc0 and 4i+2, 4i+3 in acc1 (four partial
-                // sums, two fp32 lanes each), added at the end
-                uint64_t acc0 = 0, acc1 = 0;
+            for (int qq = 0; qq < 2; ++qq) {
+              const int j = 2 * pair + qq;
+              const int q = rbase + j;
+              const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + q * kHeads);
+              // heads 4i, 4i+1 accumulate in acc0 and 4i+2, 4i+3 in acc1 (four partial
+              // sums, two fp32 lanes each), added at the end
+              uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-                for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-                  const ulonglong2 ww = wv[h4];
-                  const float x0 = __uint_as_float(cur[qq][4 * h4 + 0]);
-                  const float x1 = __uint_as_float(cur[qq][4 * h4 + 1]);
-                  const float x2 = __uint_as_float(cur[qq][4 * h4 + 2]);
-                  const float x3 = __uint_as_float(cur[qq][4 * h4 + 3]);
-                  acc0 = ptx::fma_f32x2(ww.x, ptx::pack_f32x2(fmaxf(kNegScale ? -x0 : x0, 0.0f),
-                                                              fmaxf(kNegScale ? -x1 : x1, 0.0f)), acc0);
-                  acc1 = ptx::fma_f32x2(ww.y, ptx::pack_f32x2(fmaxf(kNegScale ? -x2 : x2, 0.0f),
-                                                              fmaxf(kNegScale ? -x3 : x3, 0.0f)), acc1);
-                }
-                float s0, s1, s2, s3;
-                ptx::unpack_f32x2(acc0, s0, s1);
-                ptx::unpack_f32x2(acc1, s2, s3);
-                const float s = (s0 + s1) + (s2 + s3);
-                key[q & 3] = make_key(s, uint32_t(p));
-                m[q & 3] = __ballot_sync(0xffffffffu, p < s_elig[q] && key[q & 3] > s_tau[q]);
+              for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+                const ulonglong2 ww = wv[h4];
+                const float x0 = __uint_as_float(cur[qq][4 * h4 + 0]);
+                const float x1 = __uint_as_float(cur[qq][4 * h4 + 1]);
+                const float x2 = __uint_as_float(cur[qq][4 * h4 + 2]);
+                const float x3 = __uint_as_float(cur[qq][4 * h4 + 3]);
+                acc0 = ptx::fma_f32x2(ww.x, ptx::pack_f32x2(fmaxf(kNegScale ? -x0 : x0, 0.0f),
+                                                            fmaxf(kNegScale ? -x1 : x1, 0.0f)), acc0);
+                acc1 = ptx::fma_f32x2(ww.y, ptx::pack_f32x2(fmaxf(kNegScale ? -x2 : x2, 0.0f),
+                                                            fmaxf(kNegScale ? -x3 : x3, 0.0f)), acc1);
               }
-              if (pair + 1 < kRows / 2) {
-                ptx::tc_wait_ld();
-                ptx::tc_reg_fence(nxt[0]);
-                ptx::tc_reg_fence(nxt[1]);
-              }
-              if (pair + 1 == kRows / 2 - 1) {  // the last pair is in registers: hand the accumulator back
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar.acc_empty + grp);
-              }
-              if (pair & 1) {  // rows 4h .. 4h+3 scored: lanes 0..3 reserve their slots with one atomic
-                const int r0 = 2 * pair - 2;
-                unsigned my_m = 0;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) my_m = lane == qq ? m[qq] : my_m;
-                int base = 0;
-                if (lane < 4) base = atomicAdd(s_count + r0 + lane, __popc(my_m));
-                over = over || (lane < 4 && base + __popc(my_m) > kCompactAt);
-                // cannot happen (kCompactAt leaves room for a round); the stores below skip it
-                if (lane < 4 && base + __popc(my_m) > kCap) record_error(hdr, KPOOL_ERR_INTERNAL);
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                  const int slot = __shfl_sync(0xffffffffu, base, qq) + __popc(m[qq] & lt_mask);
-                  if (((m[qq] >> lane) & 1u) && slot < kCap) s_cand[(r0 + qq) * kCap + slot] = key[qq];
-                }
-              }
+              float s0, s1, s2, s3;
+              ptx::unpack_f32x2(acc0, s0, s1);
+              ptx::unpack_f32x2(acc1, s2, s3);
+              const float s = (s0 + s1) + (s2 + s3);
+              key[j] = make_key(s, uint32_t(p));
+              m[j] = __ballot_sync(0xffffffffu, p < s_elig[q] && key[j] > s_tau[q]);
             }
           }
+          // lanes 0..3 reserve buffer slots for the four rows with one shared atomic
+          unsigned my_m = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) my_m = lane == j ? m[j] : my_m;
+          int base = 0;
+          if (lane < 4) base = atomicAdd(s_count + rbase + lane, __popc(my_m));
+          over = lane < 4 && base + __popc(my_m) > kCompactAt;
+          // cannot happen (kCompactAt leaves room for a tile); the stores below skip it
+          if (lane < 4 && base + __popc(my_m) > kCap) record_error(hdr, KPOOL_ERR_INTERNAL);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int slot = __shfl_sync(0xffffffffu, base, j) + __popc(m[j] & lt_mask);
+            if (((m[j] >> lane) & 1u) && slot < kCap) s_cand[(rbase + j) * kCap + slot] = key[j];
+          }
         }
-        // one barrier per round in the common case; its OR says whether any row needs
-        // compacting or a wait ran out
-        if (named_bar_or(1, 256, over || !ready || *abort_flag != 0)) {
-          if (named_bar_or(1, 256, !ready || *abort_flag != 0)) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+        // one group barrier per tile in the common case; its OR says whether any of the
+        // group's rows needs compacting or a wait ran out
+        if (named_bar_or(bar_id, 128, over || !ready || *abort_flag != 0)) {
+          if (named_bar_or(bar_id, 128, !ready || *abort_flag != 0)) {
             aborted = true;
             break;
           }
-          // all 8 warps bring each overfull row back below the compaction mark together
-          for (int q = 0; q < kRows; ++q) {
+          // the group's four warps bring each overfull row back below the mark together
+          for (int j = 0; j < 4; ++j) {
+            const int q = rbase + j;
             const int n = s_count[q];
             if (n > kCompactAt) {
               uint64_t edge;
-              const int kept = block_select_compact<kCap / 256>(s_cand + q * kCap, n, budget, kSlack, et, 1, s_sel, &edge);
-              if (et == 0) {
+              const int kept = block_select_compact<kCap / 128, 4>(s_cand + q * kCap, n, budget, kSlack, gt,
+                                                                  bar_id, sel, &edge);
+              if (gt == 0) {
                 s_count[q] = kept;
                 s_tau[q] = edge - 1;  // a key must reach the edge to matter from now on
               }
             }
           }
-          named_bar(1, 256);
+          named_bar(bar_id, 128);
         }
       }
       if (aborted) break;
-      g += uint32_t(it.n_tiles);
-      // final ranking: cut each row to its top `budget` (all 8 warps together), then
-      // warp ew sorts row ew in registers and writes it in rank order
-      for (int q = 0; q < kRows; ++q) {
+      // final ranking: cut each of the group's rows to its top `budget` (the group's
+      // four warps together), then warp wq sorts row rbase + wq and writes it
+      for (int j = 0; j < 4; ++j) {
+        const int q = rbase + j;
         const int n = s_count[q];
         if (n > budget) {
           uint64_t edge;
-          const int kept = block_select_compact<kCap / 256>(s_cand + q * kCap, n, budget, 0, et, 1, s_sel, &edge);
-          if (et == 0) s_count[q] = kept;
+          const int kept = block_select_compact<kCap / 128, 4>(s_cand + q * kCap, n, budget, 0, gt, bar_id, sel,
+                                                              &edge);
+          if (gt == 0) s_count[q] = kept;
         }
       }
-      named_bar(1, 256);
+      named_bar(bar_id, 128);
       {
-        const int row = it.t0 + ew;
+        const int q = rbase + wq;
+        const int row = it.t0 + q;
         if (row < it.len) {
-          const uint64_t* buf = s_cand + ew * kCap;
-          const int n = s_count[ew];
+          const uint64_t* buf = s_cand + q * kCap;
+          const int n = s_count[q];
           uint64_t kk[kMaxBudget / 32];
 #pragma unroll
           for (int j = 0; j < kMaxBudget / 32; ++j) {
@@ -548,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       }
-      named_bar(1, 256);
+      named_bar(bar_id, 128);
     }
     ptx::tc_fence_before();
   }
