@@ -286,19 +286,59 @@ struct SelectScratch {
 // barriers instead of one warp's long dependent chain. Returns the kept count
 // (between budget and budget + slack, or all keys when n <= budget); *edge_out
 // gets the edge. Ends with a barrier: buf and the count are consistent for all.
-template <int kPer, int kWarps>
-__device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int slack, int et, int bar_id,
-                                           SelectScratch* sc, uint64_t* edge_out) {
+// Where a candidate buffer's keys live. Contiguous: slots [0, n). Quartered: four
+// regions of kReg slots, region r holding counts[r] keys (one region per warp of
+// an epilogue group, so insertion needs no atomics); the kept keys are written
+// back as four consecutive blocks, region r receiving region_count(kept, r) =
+// kept / 4 (+1 for r < kept % 4) of them, so the regions restart level and a
+// warp's 32 consecutive keys land in consecutive slots (no bank conflicts).
+// load<kT, j>(buf, t): the j-th key of thread t of kT, i.e. slot t + kT * j.
+struct ContiguousLayout {
+  int n;
+  template <int kT, int j>
+  __device__ __forceinline__ uint64_t load(const uint64_t* buf, int t) const {
+    return t + kT * j < n ? buf[t + kT * j] : 0ull;
+  }
+  __device__ __forceinline__ int pos(int e, int) const { return e; }
+};
+
+template <int kReg>
+struct QuarteredLayout {
+  const int32_t* counts;  // 4 region counts (shared memory)
+  template <int kT, int j>
+  __device__ __forceinline__ uint64_t load(const uint64_t* buf, int t) const {
+    static_assert(kReg % kT == 0, "a thread's slot t + kT * j stays in one region for every t < kT");
+    constexpr int r = kT * j / kReg, off = kT * j % kReg;  // region and offset of thread 0's slot
+    return off + t < counts[r] ? buf[kT * j + t] : 0ull;
+  }
+  // slot of kept key e (0 <= e < kept); callers keep kept <= 4 * kReg
+  __device__ __forceinline__ int pos(int e, int kept) const {
+    const int q = kept >> 2, rem = kept & 3;
+    const int s1 = q + (rem > 0), s2 = 2 * q + min(rem, 2), s3 = 3 * q + rem;  // block starts
+    const int r = (e >= s1) + (e >= s2) + (e >= s3);
+    const int start = r * q + min(r, rem);
+    return r * kReg + (e - start);
+  }
+  __device__ __forceinline__ static int region_count(int kept, int r) { return (kept >> 2) + (r < (kept & 3)); }
+};
+
+template <class Layout, int kT, int kPer, int j = 0>
+__device__ __forceinline__ void load_keys(const Layout& layout, const uint64_t* buf, int t, uint64_t (&k)[kPer]) {
+  if constexpr (j < kPer) {
+    k[j] = layout.template load<kT, j>(buf, t);
+    load_keys<Layout, kT, kPer, j + 1>(layout, buf, t, k);
+  }
+}
+
+template <int kPer, int kWarps, class Layout>
+__device__ inline int block_select_compact_in(uint64_t* buf, int n, int budget, int slack, int et, int bar_id,
+                                              SelectScratch* sc, uint64_t* edge_out, Layout layout) {
   static_assert(kWarps <= 8, "SelectScratch holds 8 warps");
   constexpr int kT = 32 * kWarps;
   const int lane = et & 31, wid = et >> 5;
   const unsigned full = 0xffffffffu;
   uint64_t k[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int idx = et + kT * j;
-    k[j] = idx < n ? buf[idx] : 0ull;
-  }
+  load_keys<Layout, kT, kPer>(layout, buf, et, k);
   uint64_t o = 0, a = ~0ull;
 #pragma unroll
   for (int j = 0; j < kPer; ++j)
@@ -368,7 +408,7 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
   } else if (n <= budget) {
     edge = 1;  // keep everything
   }
-  // write the kept keys back to the front of buf, in thread order
+  // write the kept keys back (front of buf, or dealt over the regions), in thread order
   unsigned m[kPer];
   int mine = 0;
 #pragma unroll
@@ -388,12 +428,20 @@ __device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int
   const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
-    if ((m[j] >> lane) & 1u) buf[off + __popc(m[j] & lt)] = k[j];
+    if ((m[j] >> lane) & 1u) buf[layout.pos(off + __popc(m[j] & lt), total)] = k[j];
     off += __popc(m[j]);
   }
   *edge_out = edge;
   group_bar(bar_id, kT);
   return total;
+}
+
+// Contiguous buffer of n keys.
+template <int kPer, int kWarps>
+__device__ inline int block_select_compact(uint64_t* buf, int n, int budget, int slack, int et, int bar_id,
+                                           SelectScratch* sc, uint64_t* edge_out) {
+  return block_select_compact_in<kPer, kWarps>(buf, n, budget, slack, et, bar_id, sc, edge_out,
+                                               ContiguousLayout{n});
 }
 
 }  // namespace kpool

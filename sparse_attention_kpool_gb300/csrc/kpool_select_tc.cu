@@ -76,6 +76,17 @@ constexpr int kMaxBudget = 512;
 // compacted once it holds more than kCap - 128 after a tile.
 constexpr int kCompactAt = kCap - kTilePools;
 static_assert(kCap % 128 == 0, "a group's cooperative compaction gives each of 128 threads kCap/128 keys");
+// Each row's buffer is split into four regions, one per warp of the owning group,
+// so a warp inserts with a register count and no atomics. A warp adds at most 32
+// candidates to a region per tile, so a row is compacted once a region passes
+// kReg - 32.
+constexpr int kReg = kCap / 4;
+constexpr int kRegMark = kReg - 32;
+// A compaction spreads the keys it keeps evenly over the four regions: a round's
+// keeps at most budget + slack keys, the final one at most budget.
+constexpr int kFinalChunk = kMaxBudget / 4;  // most keys a region holds after the final compaction
+static_assert(kMaxBudget % 128 == 0 && kFinalChunk % 32 == 0, "the final sort reads whole warps per region");
+static_assert((kMaxBudget + KPOOL_TC_SLACK + 3) / 4 < kRegMark, "a compaction must free room in every region");
 constexpr int kSlack = KPOOL_TC_SLACK;    // a compaction keeps between budget and budget + kSlack keys
 static_assert(kMaxBudget + kSlack < kCompactAt, "a compaction must free room for the next round");
 constexpr int kThreads = 320;
@@ -93,8 +104,8 @@ constexpr uint32_t kOffCand = kOffPool + kStages * kStageBytes;
 constexpr uint32_t kOffW = kOffCand + kRows * kCap * 8;
 constexpr uint32_t kOffBar = kOffW + kRows * kHeads * 4;
 constexpr int kNumBars = 2 + 2 * kStages + 4 + 1;
-constexpr uint32_t kOffCount = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffTau = (kOffCount + kRows * 4 + 7) & ~7u;
+constexpr uint32_t kOffCount = kOffBar + kNumBars * 8;         // [kRows][4] region counts
+constexpr uint32_t kOffTau = (kOffCount + kRows * 4 * 4 + 7) & ~7u;
 constexpr uint32_t kOffElig = kOffTau + kRows * 8;
 constexpr uint32_t kOffMisc = kOffElig + kRows * 4;
 constexpr uint32_t kOffSelect = kOffMisc + 16;              // SelectScratch
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Bars bar = bars_at(smem);
-  int32_t* s_count = reinterpret_cast<int32_t*>(smem + kOffCount);
+  int32_t* s_count = reinterpret_cast<int32_t*>(smem + kOffCount);  // [row][region]
   uint64_t* s_tau = reinterpret_cast<uint64_t*>(smem + kOffTau);
   int32_t* s_elig = reinterpret_cast<int32_t*>(smem + kOffElig);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -385,10 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gt < 4) {
         const int q = rbase + gt;
         const int row = it.t0 + q;
-        s_count[q] = 0;
         s_tau[q] = 0;
         s_elig[q] = row < it.len ? (row + 1) / kpool : 0;
       }
+      int cnt[4] = {0, 0, 0, 0};  // this warp's region counts of the group's four rows
       named_bar(bar_id, 128);
       bool aborted = false;
       for (int i = 0; i < it.n_tiles; ++i) {
@@ -403,110 +414,119 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const int p = i * kTilePools + lg * 32 + lane;  // sequence-local pool index of this thread
           const uint32_t col0 = lane_addr + uint32_t(acc * kAccCols + rbase * kHeads);
-          // TMEM -> registers two rows at a time; the second pair is in flight while
-          // the first is scored.
-          uint32_t va[2][32], vb[2][32];
+          // TMEM -> registers one row at a time; the next row's columns and head
+          // weights are in flight while the current row is scored.
+          uint32_t v[2][32];
+          ulonglong2 wr[2][kHeads / 4];
           uint64_t key[4];
           unsigned m[4];
-          ptx::tc_ld_32x32b_x32(col0 + 0 * kHeads, va[0]);
-          ptx::tc_ld_32x32b_x32(col0 + 1 * kHeads, va[1]);
-          ptx::tc_wait_ld();
-          ptx::tc_reg_fence(va[0]);
-          ptx::tc_reg_fence(va[1]);
-          ptx::tc_ld_32x32b_x32(col0 + 2 * kHeads, vb[0]);
-          ptx::tc_ld_32x32b_x32(col0 + 3 * kHeads, vb[1]);
+          ptx::tc_ld_32x32b_x32(col0, v[0]);
+          {
+            const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + rbase * kHeads);
 #pragma unroll
-          for (int pair = 0; pair < 2; ++pair) {
-            uint32_t (&cur)[2][32] = pair ? vb : va;
-            if (pair == 1) {
-              ptx::tc_wait_ld();
-              ptx::tc_reg_fence(vb[0]);
-              ptx::tc_reg_fence(vb[1]);
+            for (int h4 = 0; h4 < kHeads / 4; ++h4) wr[0][h4] = wv[h4];
+          }
+          ptx::tc_wait_ld();
+          ptx::tc_reg_fence(v[0]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int q = rbase + j;
+            if (j < 3) {
+              ptx::tc_ld_32x32b_x32(col0 + (j + 1) * kHeads, v[(j + 1) & 1]);
+              const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + (q + 1) * kHeads);
+#pragma unroll
+              for (int h4 = 0; h4 < kHeads / 4; ++h4) wr[(j + 1) & 1][h4] = wv[h4];
+            } else {
               // every column this warp needs is in registers: release the accumulator
               ptx::tc_fence_before();
               __syncwarp();
               if (lane == 0) ptx::mbar_arrive(bar.acc_empty + acc);
             }
+            const uint32_t (&cur)[32] = v[j & 1];
+            const ulonglong2 (&wc)[kHeads / 4] = wr[j & 1];
+            uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-              const int j = 2 * pair + qq;
-              const int q = rbase + j;
-              const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + q * kHeads);
-              // heads 4i, 4i+1 accumulate in acc0 and 4i+2, 4i+3 in acc1 (four partial
-              // sums, two fp32 lanes each), added at the end
-              uint64_t acc0 = 0, acc1 = 0;
-#pragma unroll
-              for (int h4 = 0; h4 < kHeads / 4; ++h4) {
-                const ulonglong2 ww = wv[h4];
-                const float x0 = __uint_as_float(cur[qq][4 * h4 + 0]);
-                const float x1 = __uint_as_float(cur[qq][4 * h4 + 1]);
-                const float x2 = __uint_as_float(cur[qq][4 * h4 + 2]);
-                const float x3 = __uint_as_float(cur[qq][4 * h4 + 3]);
-                acc0 = ptx::fma_f32x2(ww.x, ptx::pack_f32x2(fmaxf(kNegScale ? -x0 : x0, 0.0f),
-                                                            fmaxf(kNegScale ? -x1 : x1, 0.0f)), acc0);
-                acc1 = ptx::fma_f32x2(ww.y, ptx::pack_f32x2(fmaxf(kNegScale ? -x2 : x2, 0.0f),
-                                                            fmaxf(kNegScale ? -x3 : x3, 0.0f)), acc1);
-              }
-              float s0, s1, s2, s3;
-              ptx::unpack_f32x2(acc0, s0, s1);
-              ptx::unpack_f32x2(acc1, s2, s3);
-              const float s = (s0 + s1) + (s2 + s3);
-              key[j] = make_key(s, uint32_t(p));
-              m[j] = __ballot_sync(0xffffffffu, p < s_elig[q] && key[j] > s_tau[q]);
+            for (int h4 = 0; h4 < kHeads / 4; ++h4) {
+              const ulonglong2 ww = wc[h4];
+              const float x0 = __uint_as_float(cur[4 * h4 + 0]);
+              const float x1 = __uint_as_float(cur[4 * h4 + 1]);
+              const float x2 = __uint_as_float(cur[4 * h4 + 2]);
+              const float x3 = __uint_as_float(cur[4 * h4 + 3]);
+              acc0 = ptx::fma_f32x2(ww.x, ptx::pack_f32x2(fmaxf(kNegScale ? -x0 : x0, 0.0f),
+                                                          fmaxf(kNegScale ? -x1 : x1, 0.0f)), acc0);
+              acc1 = ptx::fma_f32x2(ww.y, ptx::pack_f32x2(fmaxf(kNegScale ? -x2 : x2, 0.0f),
+                                                          fmaxf(kNegScale ? -x3 : x3, 0.0f)), acc1);
+            }
+            float s0, s1, s2, s3;
+            ptx::unpack_f32x2(acc0, s0, s1);
+            ptx::unpack_f32x2(acc1, s2, s3);
+            const float s = (s0 + s1) + (s2 + s3);
+            key[j] = make_key(s, uint32_t(p));
+            m[j] = __ballot_sync(0xffffffffu, p < s_elig[q] && key[j] > s_tau[q]);
+            if (j < 3) {
+              ptx::tc_wait_ld();
+              ptx::tc_reg_fence(v[(j + 1) & 1]);
             }
           }
-          // lanes 0..3 reserve buffer slots for the four rows with one shared atomic
-          unsigned my_m = 0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) my_m = lane == j ? m[j] : my_m;
-          int base = 0;
-          if (lane < 4) base = atomicAdd(s_count + rbase + lane, __popc(my_m));
-          over = lane < 4 && base + __popc(my_m) > kCompactAt;
-          // cannot happen (kCompactAt leaves room for a tile); the stores below skip it
-          if (lane < 4 && base + __popc(my_m) > kCap) record_error(hdr, KPOOL_ERR_INTERNAL);
+          // append to this warp's region of each row (warp-uniform counts, no atomics)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int slot = __shfl_sync(0xffffffffu, base, j) + __popc(m[j] & lt_mask);
-            if (((m[j] >> lane) & 1u) && slot < kCap) s_cand[(rbase + j) * kCap + slot] = key[j];
+            const int slot = cnt[j] + __popc(m[j] & lt_mask);
+            if (((m[j] >> lane) & 1u) && slot < kReg) s_cand[(rbase + j) * kCap + wq * kReg + slot] = key[j];
+            cnt[j] += __popc(m[j]);
+            over = over || cnt[j] > kRegMark;
           }
+          // cannot happen (kRegMark leaves room for a tile); the stores above skip it
+          if (lane == 0 && (cnt[0] > kReg || cnt[1] > kReg || cnt[2] > kReg || cnt[3] > kReg))
+            record_error(hdr, KPOOL_ERR_INTERNAL);
         }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
         // one group barrier per tile in the common case; its OR says whether any of the
         // group's rows needs compacting or a wait ran out
         if (named_bar_or(bar_id, 128, over || !ready || *abort_flag != 0)) {
+          if (lane == 0)  // publish this warp's region counts for the cooperative compaction
+            for (int j = 0; j < 4; ++j) s_count[(rbase + j) * 4 + wq] = cnt[j];
           if (named_bar_or(bar_id, 128, !ready || *abort_flag != 0)) {
             aborted = true;
             break;
           }
-          // the group's four warps bring each overfull row back below the mark together
+          // the group's four warps bring each row with a full region back down together
           for (int j = 0; j < 4; ++j) {
             const int q = rbase + j;
-            const int n = s_count[q];
-            if (n > kCompactAt) {
+            const int32_t* c = s_count + q * 4;
+            if (max(max(c[0], c[1]), max(c[2], c[3])) > kRegMark) {
               uint64_t edge;
-              const int kept = block_select_compact<kCap / 128, 4>(s_cand + q * kCap, n, budget, kSlack, gt,
-                                                                  bar_id, sel, &edge);
-              if (gt == 0) {
-                s_count[q] = kept;
-                s_tau[q] = edge - 1;  // a key must reach the edge to matter from now on
-              }
+              using L = QuarteredLayout<kReg>;
+              const int kept = block_select_compact_in<kCap / 128, 4>(
+                  s_cand + q * kCap, c[0] + c[1] + c[2] + c[3], budget, kSlack, gt, bar_id, sel, &edge, L{c});
+              if (gt < 4) s_count[q * 4 + gt] = L::region_count(kept, gt);
+              if (gt == 0) s_tau[q] = edge - 1;  // a key must reach the edge to matter from now on
             }
           }
           named_bar(bar_id, 128);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cnt[j] = s_count[(rbase + j) * 4 + wq];
         }
       }
       if (aborted) break;
-      // final ranking: cut each of the group's rows to its top `budget` (the group's
-      // four warps together), then warp wq sorts row rbase + wq and writes it
+      // final ranking: cut each of the group's rows to its top `budget` keys, dealt
+      // evenly over the four regions (the group's four warps together), then warp wq
+      // sorts row rbase + wq and writes it
+      if (lane == 0)
+        for (int j = 0; j < 4; ++j) s_count[(rbase + j) * 4 + wq] = cnt[j];
+      named_bar(bar_id, 128);
       for (int j = 0; j < 4; ++j) {
         const int q = rbase + j;
-        const int n = s_count[q];
-        if (n > budget) {
+        const int32_t* c = s_count + q * 4;
+        const int n = c[0] + c[1] + c[2] + c[3];
+        // the sort below reads the first kFinalChunk slots of each region
+        if (n > budget || max(max(c[0], c[1]), max(c[2], c[3])) > kFinalChunk) {
+          using L = QuarteredLayout<kReg>;
           uint64_t edge;
-          const int kept = block_select_compact<kCap / 128, 4>(s_cand + q * kCap, n, budget, 0, gt, bar_id, sel,
-                                                              &edge);
-          if (gt == 0) s_count[q] = kept;
+          const int kept = block_select_compact_in<kCap / 128, 4>(s_cand + q * kCap, n, budget, 0, gt, bar_id, sel,
+                                                                 &edge, L{c});
+          if (gt < 4) s_count[q * 4 + gt] = L::region_count(kept, gt);
         }
       }
       named_bar(bar_id, 128);
@@ -515,12 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = it.t0 + q;
         if (row < it.len) {
           const uint64_t* buf = s_cand + q * kCap;
-          const int n = s_count[q];
+          const int32_t* c = s_count + q * 4;
           uint64_t kk[kMaxBudget / 32];
 #pragma unroll
           for (int j = 0; j < kMaxBudget / 32; ++j) {
-            const int e = 32 * j + lane;
-            kk[j] = e < n ? buf[e] : 0ull;
+            constexpr int kPerRegion = kFinalChunk / 32;
+            const int r = j / kPerRegion, off = (j % kPerRegion) * 32 + lane;  // region, offset
+            kk[j] = off < c[r] ? buf[r * kReg + off] : 0ull;
           }
           warp_sort512_blocked_desc(kk);  // lane l now holds ranks 16 l .. 16 l + 15
           const int64_t grow = it.seq_start + row;
