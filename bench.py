@@ -50,7 +50,10 @@ FLOP_PER_PAIR_PER_HEAD_DIM = 2  # one multiply-add per (head, channel) of a scor
 # DRAM traffic of the score+select kernel from one ncu capture, per launch at the
 # pages-scale workload, tied to the kernel source it was measured on: when the
 # source hash differs the number is stale and is reported as null.
-NCU_TRAFFIC = {"kernel_sha256": None, "workload": None, "bytes_per_launch": None}
+NCU_TRAFFIC = {"kernel_sha256": "6d7665ec01737c94", "workload": "pages_512k",
+               # long_128k capture: 1.104 GB read + 0.212 GB written per launch; q, w and the
+               # pool ids grow with the rows, so x4 at 524288 tokens
+               "bytes_per_launch": 4 * (1.104467e9 + 0.212411e9)}
 
 
 def source_sha(path: str) -> str:
@@ -195,6 +198,16 @@ def pick_sample_rows(wl: W.Workload, target_pairs: float, seed: int) -> np.ndarr
     return np.array(sorted(set(rows)), dtype=np.int64)
 
 
+def workload_config(wl: W.Workload, world: int) -> dict:
+    """The `config` object of the JSON line, identical for both arms."""
+    return {"workload": wl.name, "seqlens": list(wl.seqlens) if len(wl.seqlens) <= 8 else wl.num_seqs,
+            "heads": wl.heads, "head_dim": wl.head_dim, "kpool": wl.kpool, "index_topk": wl.index_topk,
+            "budget": wl.budget, "scale": wl.scale,
+            "inputs": "q,k %s N(0,1), w fp32 U(0,1), seeded (CUDA Philox)" % wl.dtype,
+            "l2": "inputs larger than L2 (q alone is %.1f GiB)" % (wl.total_tokens * wl.heads * wl.head_dim * 2 / 2**30),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def reference_arm(args, wl, world, rank):
     """The oracle as the reference implementation: each step scores a bounded row sample."""
     if rank != 0:
@@ -219,9 +232,7 @@ def reference_arm(args, wl, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "seqlens": list(wl.seqlens), "heads": wl.heads, "head_dim": wl.head_dim,
-                   "kpool": wl.kpool, "index_topk": wl.index_topk, "budget": wl.budget,
-                   "inputs": "q,k bf16 N(0,1), w fp32 U(0,1), seeded"},
+        "config": workload_config(wl, world),
         "sec_per_selection_extrapolated": wl.causal_pairs() / value,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
                          "sample": f"{len(times)} steps x ~{args.ref_pairs_per_step:.2e} pairs of uniform rows "
@@ -363,11 +374,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "seqlens": list(wl.seqlens) if len(wl.seqlens) <= 8 else wl.num_seqs,
-                   "heads": H, "head_dim": d, "kpool": wl.kpool, "index_topk": wl.index_topk, "budget": B,
-                   "scale": wl.scale, "inputs": "q,k bf16 N(0,1), w fp32 U(0,1), seeded (CUDA Philox)",
-                   "l2": "inputs larger than L2 (q alone is %.1f GiB)" % (inp["q"].numel() * 2 / 2**30),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(wl, world),
         "sec_per_selection": ms_step / 1e3,
         "scored_pairs_per_s": value,
         "pct_bf16_peak": 100.0 * achieved / peak_sust,
