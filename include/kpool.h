@@ -142,6 +142,41 @@ kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, in
                           int32_t* out_token_ids, void* stream);
 
 /*
+ * Selection for an explicit set of query rows against pooled keys that already
+ * exist: the decode / short-query case, where a few new query tokens score a
+ * long pooled-key cache ("spark_model/layers/glm5next_dsa/tp.rs", module docs,
+ * "Why the indexer is REPLICATED": at a 262,144-token context one decode token
+ * scores n_pools = 65,536 pools). Row r sits at sequence-local position
+ * row_pos[r] of sequence row_seq[r] of the key batch described by cu_seqlens,
+ * and gets exactly what row row_pos[r] of kpool_select would get for a query
+ * q[r] with weights w[r]: the top budget of the pools p < floor((t+1)/kpool) of
+ * its sequence (higher score, then smaller pool index), -1 padded, rank order,
+ * expanded to token ids with its incomplete trailing pool appended.
+ *   q               [R, H, d] dtype (16-byte aligned); row r is that row's query.
+ *   w               [R, H] fp32.
+ *   row_seq, row_pos [R] int32 (device): 0 <= row_seq < S, 0 <= row_pos < L_b.
+ *   pooled_keys     [P, d] dtype, as kpool_pool_keys writes them for cu_seqlens
+ *                   (16-byte aligned; may be NULL only when T / kpool == 0).
+ *   cu_seqlens      [S + 1] int32 of the key sequences, as for kpool_pool_keys.
+ *   out_pool_ids    [R, budget] int32; out_token_ids [R, index_topk + kpool] int32;
+ *   out_pool_scores [R, budget] fp32 or NULL.
+ *   workspace       >= kpool_rows_workspace_bytes(R, T, S, kpool, index_topk) bytes.
+ * Supported: bf16, H = 32, d = 128, budget <= 512 (else KPOOL_ERR_UNSUPPORTED).
+ * R = 0 is a valid no-op. A row whose row_seq or row_pos is out of range gets
+ * all -1 outputs and the call records KPOOL_ERR_INVALID_ARG on the device
+ * (kpool_last_device_error); malformed cu_seqlens records the same and every
+ * row gets -1 outputs.
+ */
+size_t kpool_rows_workspace_bytes(int32_t num_rows, int64_t total_tokens, int32_t num_seqs, int32_t kpool,
+                                  int32_t index_topk);
+kpool_status kpool_select_rows(const void* q, const float* w, const int32_t* row_seq, const int32_t* row_pos,
+                               int32_t num_rows, const void* pooled_keys, const int32_t* cu_seqlens,
+                               int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                               kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                               int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads the device error word the last call on this
  * workspace recorded: KPOOL_OK, KPOOL_ERR_INVALID_ARG (malformed cu_seqlens),
  * KPOOL_ERR_DEVICE_TIMEOUT (a bounded wait ran out), KPOOL_ERR_INTERNAL (a

@@ -220,6 +220,47 @@ kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, in
   return KPOOL_OK;
 }
 
+size_t kpool_rows_workspace_bytes(int32_t num_rows, int64_t total_tokens, int32_t num_seqs, int32_t kpool,
+                                  int32_t index_topk) {
+  if (num_rows < 0 || total_tokens < 0 || total_tokens > int64_t(INT32_MAX) || num_seqs < 0 ||
+      (total_tokens > 0 && num_seqs < 1))
+    return 0;
+  if (kpool < 1 || index_topk < 0 || index_topk % kpool != 0) return 0;
+  return rows_layout(num_rows, total_tokens, num_seqs, kpool).total;
+}
+
+kpool_status kpool_select_rows(const void* q, const float* w, const int32_t* row_seq, const int32_t* row_pos,
+                               int32_t num_rows, const void* pooled_keys, const int32_t* cu_seqlens,
+                               int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                               kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                               int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                               void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
+  if (st != KPOOL_OK) return st;
+  if (num_rows < 0 || heads < 1 || index_topk < 0 || index_topk % kpool != 0 || !isfinite(scale))
+    return KPOOL_ERR_INVALID_ARG;
+  if (num_rows == 0) return KPOOL_OK;
+  if (total_tokens == 0) return KPOOL_ERR_INVALID_ARG;  // a row needs a sequence to sit in
+  const int32_t budget = index_topk / kpool;
+  if (!q || !w || !row_seq || !row_pos || !cu_seqlens || !out_token_ids || (budget > 0 && !out_pool_ids) ||
+      (total_tokens / kpool > 0 && !pooled_keys))
+    return KPOOL_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(pooled_keys, 16) || !aligned(w, 4) || !aligned(row_seq, 4) ||
+      !aligned(row_pos, 4) || !aligned(cu_seqlens, 4) || !aligned(out_pool_ids, 4) ||
+      !aligned(out_token_ids, 4) || !aligned(out_pool_scores, 4))
+    return KPOOL_ERR_INVALID_ARG;
+  if (!select_rows_supported(dtype, heads, head_dim, budget)) return KPOOL_ERR_UNSUPPORTED;
+  const RowsLayout L = rows_layout(num_rows, total_tokens, num_seqs, kpool);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < L.total) return KPOOL_ERR_WORKSPACE;
+  int sms = 0;
+  if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_select_rows(q, w, row_seq, row_pos, num_rows, pooled_keys, cu_seqlens, num_seqs,
+                                  total_tokens, kpool, budget, scale, out_pool_ids, out_pool_scores, out_token_ids,
+                                  static_cast<char*>(workspace), L, sms, static_cast<cudaStream_t>(stream_ptr))))
+    return KPOOL_ERR_CUDA;
+  return KPOOL_OK;
+}
+
 kpool_status kpool_last_device_error(const void* workspace, void* stream_ptr) {
   if (workspace == nullptr || !aligned(workspace, 256)) return KPOOL_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);

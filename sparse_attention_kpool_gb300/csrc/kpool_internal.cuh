@@ -124,6 +124,20 @@ cudaError_t launch_expand(const int32_t* pool_ids, const int32_t* cu, int32_t S,
                           int32_t budget, int32_t* out_tokens, const WorkspaceHeader* hdr, int num_sms,
                           cudaStream_t stream);
 
+// Selection for explicit query rows against an existing pooled-key cache
+// (kpool_rows.cu): workspace layout, shape support and the R0-R2 launches.
+struct RowsLayout {
+  size_t header, pool_off, info, unit_off, scores, total;
+  int64_t stride;  // floats per row of the score buffer (>= T / kpool, multiple of 4)
+};
+RowsLayout rows_layout(int32_t R, int64_t T, int32_t S, int32_t kpool);
+bool select_rows_supported(kpool_dtype dtype, int32_t H, int32_t d, int32_t budget);
+cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row_seq, const int32_t* row_pos,
+                               int32_t R, const void* kp, const int32_t* cu, int32_t S, int64_t T, int32_t kpool,
+                               int32_t budget, float scale, int32_t* out_ids, float* out_scores,
+                               int32_t* out_tokens, char* ws, const RowsLayout& L, int num_sms,
+                               cudaStream_t stream);
+
 // Bounded-wait self test.
 cudaError_t launch_wait_selftest(char* ws, int64_t spin_limit, cudaStream_t stream);
 

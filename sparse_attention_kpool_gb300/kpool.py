@@ -38,7 +38,7 @@ KPOOL_SCORE_SIMT = 2
 EXPORTED = (
     "kpool_workspace_bytes", "kpool_select", "kpool_select_ex", "kpool_pool_keys", "kpool_expand",
     "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string", "kpool_last_cuda_error",
-    "kpool_select_static_scratch",
+    "kpool_select_static_scratch", "kpool_rows_workspace_bytes", "kpool_select_rows",
 )
 KPOOL_STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -95,6 +95,11 @@ def load() -> ctypes.CDLL:
         lib.kpool_last_cuda_error.restype = ctypes.c_char_p
         lib.kpool_select_static_scratch.argtypes = [P, P, P, P, i32, i64, i32, i32, i32, i32, i32, f32, P, P, P, P]
         lib.kpool_select_static_scratch.restype = i32
+        lib.kpool_rows_workspace_bytes.argtypes = [i32, i64, i32, i32, i32]
+        lib.kpool_rows_workspace_bytes.restype = sz
+        lib.kpool_select_rows.argtypes = [P, P, P, P, i32, P, P, i32, i64, i32, i32, i32, i32, i32, f32, P, P, P,
+                                          P, sz, P]
+        lib.kpool_select_rows.restype = i32
         _lib = lib
         return lib
 
@@ -256,4 +261,53 @@ def kpool_select_static_scratch(q: torch.Tensor, k: torch.Tensor, w: torch.Tenso
                                             _ptr(out_pool_scores), _stream(stream))
     if st != KPOOL_OK:
         raise KpoolError(st, "kpool_select_static_scratch")
+    return out_pool_ids, out_token_ids, out_pool_scores
+
+
+def kpool_rows_workspace_bytes(num_rows: int, total_tokens: int, num_seqs: int, kpool: int, index_topk: int) -> int:
+    return int(load().kpool_rows_workspace_bytes(num_rows, total_tokens, num_seqs, kpool, index_topk))
+
+
+def new_rows_workspace(num_rows: int, total_tokens: int, num_seqs: int, kpool: int, index_topk: int,
+                       device=None) -> torch.Tensor:
+    n = kpool_rows_workspace_bytes(num_rows, total_tokens, num_seqs, kpool, index_topk)
+    if n == 0:
+        raise KpoolError(KPOOL_ERR_INVALID_ARG, "kpool_rows_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def kpool_select_rows(q: torch.Tensor, w: torch.Tensor, row_seq: torch.Tensor, row_pos: torch.Tensor,
+                      pooled_keys: torch.Tensor, cu_seqlens: torch.Tensor, total_tokens: int, kpool: int,
+                      index_topk: int, scale: float, out_pool_ids=None, out_token_ids=None, out_pool_scores=None,
+                      return_scores: bool = False, workspace=None, stream=None):
+    """Selection for explicit query rows against an existing pooled-key cache (decode).
+
+    q [R,H,d] bf16, w [R,H] fp32, row_seq / row_pos [R] int32 (sequence and local position of
+    each row), pooled_keys [>= P, d] as kpool_pool_keys returns them for cu_seqlens [S+1]
+    (the key batch of total_tokens tokens) -> (pool_ids [R,B], token_ids [R, index_topk+kpool],
+    pool_scores [R,B] or None)."""
+    R, H, d = q.shape
+    S = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    if (pooled_keys.dtype != q.dtype or w.dtype != torch.float32 or cu_seqlens.dtype != torch.int32
+            or row_seq.dtype != torch.int32 or row_pos.dtype != torch.int32):
+        raise TypeError("pooled_keys must match q's dtype; w float32; cu_seqlens, row_seq, row_pos int32")
+    B = index_topk // kpool if kpool > 0 else 0
+    dev = q.device
+    if out_pool_ids is None:
+        out_pool_ids = torch.empty((R, B), dtype=torch.int32, device=dev)
+    if out_token_ids is None:
+        out_token_ids = torch.empty((R, index_topk + kpool), dtype=torch.int32, device=dev)
+    if out_pool_scores is None and return_scores:
+        out_pool_scores = torch.empty((R, B), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_rows_workspace(R, total_tokens, S, kpool, index_topk, dev)
+    _check_cuda(q, w, row_seq, row_pos, pooled_keys, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores,
+                workspace)
+    st = load().kpool_select_rows(_ptr(q), _ptr(w), _ptr(row_seq), _ptr(row_pos), R, _ptr(pooled_keys),
+                                  _ptr(cu_seqlens), S, int(total_tokens), H, d, dt, kpool, index_topk, float(scale),
+                                  _ptr(out_pool_ids), _ptr(out_token_ids), _ptr(out_pool_scores), _ptr(workspace),
+                                  workspace.numel(), _stream(stream))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_select_rows")
     return out_pool_ids, out_token_ids, out_pool_scores

@@ -161,3 +161,113 @@ def sample_rows(wl: Workload, count: int, seed: int = 12345) -> torch.Tensor:
         need = max(0, count - len(picks))
         picks.update(torch.randint(0, T, (need,), generator=g).tolist())
     return torch.tensor(sorted(picks), dtype=torch.int64)
+
+
+# --------------------------------------------------------------- explicit query rows
+#
+# The decode / short-query case: a few query rows, each at a position of one key
+# sequence, score that sequence's pooled-key cache. The pages' example is one
+# decode token at a 262,144-token context scoring 65,536 pools
+# ("spark_model/layers/glm5next_dsa/tp.rs", module docs, "Why the indexer is
+# REPLICATED"); a batch of such sequences stands in for a decode batch.
+
+
+@dataclass(frozen=True)
+class RowsWorkload:
+    name: str
+    seqlens: tuple        # key sequences (the cache)
+    rows: tuple           # ((seq, pos), ...) of the query rows; pos < 0 means seqlens[seq] + pos
+    heads: int
+    head_dim: int
+    kpool: int
+    index_topk: int
+    scale: float
+    dtype: str
+    values: str
+    seed: int
+    dup_every: int = 0
+    description: str = field(default="", compare=False)
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.seqlens))
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.seqlens)
+
+    @property
+    def num_rows(self) -> int:
+        return len(self.rows)
+
+    @property
+    def budget(self) -> int:
+        return self.index_topk // self.kpool
+
+    @property
+    def width(self) -> int:
+        return self.index_topk + self.kpool
+
+    def cu_seqlens(self) -> torch.Tensor:
+        return Workload("", self.seqlens, 1, 1, 1, 1, 1.0, "f32", "normal", 0).cu_seqlens()
+
+    def row_positions(self):
+        """(seq, pos) of every row with negative positions resolved."""
+        out = []
+        for b, t in self.rows:
+            out.append((int(b), int(t) if t >= 0 else int(self.seqlens[b]) + int(t)))
+        return out
+
+    def global_rows(self):
+        cu = self.cu_seqlens().tolist()
+        return [cu[b] + t for b, t in self.row_positions()]
+
+    def scored_pairs(self) -> int:
+        return sum((t + 1) // self.kpool for _, t in self.row_positions())
+
+
+DECODE_SMALL = RowsWorkload(
+    "decode_small", (5000, 12345, 2, 8191),
+    ((0, -1), (1, -1), (3, -1), (2, 1), (0, 0), (0, 2), (0, 3), (1, 2047), (1, 2048), (1, 6000), (3, 4099),
+     (3, 4095), (1, -2), (0, 1234), (3, 2049), (1, -1)),
+    32, 128, 4, 2048, _S128, "bf16", "normal", 11,
+    description="Decode rows against four key caches (5000/12345/2/8191 tokens) at assorted positions")
+DECODE_TIE = RowsWorkload(
+    "decode_tie", (4096, 6000),
+    ((0, -1), (1, -1), (0, 2051), (1, 4999), (0, 100), (1, -3)),
+    32, 128, 4, 2048, 1.0 / 16.0, "bf16", "integer", 12, dup_every=8,
+    description="Integer-valued decode rows with duplicated pools (exact ties at the cutoff)")
+DECODE_262K = RowsWorkload(
+    "decode_262k", (262144,) * 16, tuple((b, -1) for b in range(16)),
+    32, 128, 4, 2048, _S128, "bf16", "normal", 13,
+    description="Decode batch: 16 sequences x 262,144-token caches, one new query row each (65,536 pools)")
+
+ROWS_ALL = (DECODE_SMALL, DECODE_TIE, DECODE_262K)
+ROWS_BY_NAME = {w.name: w for w in ROWS_ALL}
+
+
+def generate_rows(wl: RowsWorkload, device="cpu") -> dict:
+    """Draw the key cache k [T,d], cu_seqlens, and the rows' q [R,H,d], w [R,H], row_seq, row_pos."""
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed)
+    T, H, d, R = wl.total_tokens, wl.heads, wl.head_dim, wl.num_rows
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    if wl.values == "normal":
+        k = torch.randn((T, d), generator=g, device=device, dtype=torch.float32).to(tdt)
+        q = torch.randn((R, H, d), generator=g, device=device, dtype=torch.float32).to(tdt)
+        w = torch.rand((R, H), generator=g, device=device, dtype=torch.float32)
+    elif wl.values == "integer":
+        k = torch.randint(-2, 3, (T, d), generator=g, device=device, dtype=torch.int32).to(tdt)
+        q = torch.randint(-2, 3, (R, H, d), generator=g, device=device, dtype=torch.int32).to(tdt)
+        w = torch.randint(0, 5, (R, H), generator=g, device=device, dtype=torch.int32).to(torch.float32) / 4.0
+    else:
+        raise ValueError(f"unknown value recipe {wl.values!r}")
+    cu = wl.cu_seqlens()
+    if wl.dup_every > 0:
+        _plant_duplicate_pools(k, cu, wl.kpool, wl.dup_every, wl.seed)
+    pos = wl.row_positions()
+    row_seq = torch.tensor([b for b, _ in pos], dtype=torch.int32)
+    row_pos = torch.tensor([t for _, t in pos], dtype=torch.int32)
+    return {"k": k, "q": q, "w": w, "cu_seqlens": cu.to(device), "row_seq": row_seq.to(device),
+            "row_pos": row_pos.to(device)}

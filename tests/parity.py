@@ -47,8 +47,11 @@ def _tol(s_ref_row: np.ndarray, s: float) -> float:
 
 
 def compare_float(inp: dict, wl, ref: dict, gpu_ids: np.ndarray, gpu_scores: np.ndarray | None,
-                  gpu_tokens: np.ndarray) -> dict:
-    """Apply the tolerance rule to the rows in ref["rows"]; returns counters. Raises AssertionError."""
+                  gpu_tokens: np.ndarray, q_rows=None, w_rows=None) -> dict:
+    """Apply the tolerance rule to the rows in ref["rows"]; returns counters. Raises AssertionError.
+
+    The query and weights of ref row i are inp["q"][row], inp["w"][row] (a packed batch), or
+    q_rows[i], w_rows[i] when those are given (explicit query rows)."""
     cu = inp["cu_seqlens"].cpu().numpy()
     kp = ref["kp"]
     B = wl.budget
@@ -70,9 +73,12 @@ def compare_float(inp: dict, wl, ref: dict, gpu_ids: np.ndarray, gpu_scores: np.
             same = False
         b = int(np.searchsorted(cu, row, side="right") - 1)
         pool0 = int(oracle.pool_offsets(cu, wl.kpool)[b])
-        if row not in q_cpu_cache:
-            q_cpu_cache[row] = (bits(inp["q"][row]), inp["w"][row].cpu().numpy())
-        qr, wr = q_cpu_cache[row]
+        if q_rows is not None:
+            qr, wr = bits(q_rows[i]), w_rows[i].cpu().numpy()
+        else:
+            if row not in q_cpu_cache:
+                q_cpu_cache[row] = (bits(inp["q"][row]), inp["w"][row].cpu().numpy())
+            qr, wr = q_cpu_cache[row]
 
         def s_ref(p):
             return oracle.score(qr, wr, kp[pool0 + p], wl.dtype, wl.scale)

@@ -137,6 +137,47 @@ def test_selftest_and_error_query_validation(lib):
     assert lib.kpool_last_device_error(P(FAKE + 8), None) == K.KPOOL_ERR_WORKSPACE
 
 
+def _rows(lib, R=4, T=4096, S=1, H=32, d=128, dtype=K.KPOOL_BF16, kpool=4, topk=2048, scale=0.1, q=FAKE, w=FAKE,
+          rs=FAKE, rp=FAKE, kp=FAKE, cu=FAKE, ids=FAKE, toks=FAKE, ws=FAKE, ws_bytes=1 << 30):
+    P = ctypes.c_void_p
+    pp = lambda x: P(x) if x else None  # noqa: E731
+    return lib.kpool_select_rows(pp(q), pp(w), pp(rs), pp(rp), R, pp(kp), pp(cu), S, T, H, d, dtype, kpool, topk,
+                                 scale, pp(ids), pp(toks), None, pp(ws), ws_bytes, None)
+
+
+def test_rows_workspace_bytes(lib):
+    a = K.kpool_rows_workspace_bytes(16, 262144 * 16, 16, 4, 2048)
+    b = K.kpool_rows_workspace_bytes(32, 262144 * 16, 16, 4, 2048)
+    assert a > 0 and b > a and a % 256 == 0
+    # the score buffer holds T / kpool floats per row
+    assert b - a >= 16 * (262144 * 16 // 4) * 4
+    assert K.kpool_rows_workspace_bytes(-1, 100, 1, 4, 16) == 0
+    assert K.kpool_rows_workspace_bytes(4, 100, 1, 0, 16) == 0
+    assert K.kpool_rows_workspace_bytes(4, 100, 1, 3, 16) == 0
+    assert K.kpool_rows_workspace_bytes(4, 100, 0, 4, 16) == 0
+
+
+def test_select_rows_rejects_bad_arguments(lib):
+    assert _rows(lib, kpool=0) == K.KPOOL_ERR_INVALID_ARG
+    assert _rows(lib, topk=2046) == K.KPOOL_ERR_INVALID_ARG
+    assert _rows(lib, R=-1) == K.KPOOL_ERR_INVALID_ARG
+    assert _rows(lib, scale=float("nan")) == K.KPOOL_ERR_INVALID_ARG
+    assert _rows(lib, T=0, S=0) == K.KPOOL_ERR_INVALID_ARG            # rows need a sequence
+    for name in ("q", "w", "rs", "rp", "kp", "cu", "ids", "toks"):
+        assert _rows(lib, **{name: 0}) == K.KPOOL_ERR_INVALID_ARG, name
+    assert _rows(lib, q=FAKE + 8) == K.KPOOL_ERR_INVALID_ARG           # 16-byte rows for the vector loads
+    assert _rows(lib, kp=FAKE + 8) == K.KPOOL_ERR_INVALID_ARG
+    assert _rows(lib, rp=FAKE + 2) == K.KPOOL_ERR_INVALID_ARG
+    assert _rows(lib, dtype=K.KPOOL_F32, d=128) == K.KPOOL_ERR_UNSUPPORTED
+    assert _rows(lib, H=16) == K.KPOOL_ERR_UNSUPPORTED
+    assert _rows(lib, topk=4096) == K.KPOOL_ERR_UNSUPPORTED             # budget 1024 > 512
+    assert _rows(lib, ws=0) == K.KPOOL_ERR_WORKSPACE
+    assert _rows(lib, ws=FAKE + 64) == K.KPOOL_ERR_WORKSPACE
+    assert _rows(lib, ws_bytes=4096) == K.KPOOL_ERR_WORKSPACE
+    # no rows: nothing to do, nothing checked beyond the shape
+    assert _rows(lib, R=0, q=0, w=0, rs=0, rp=0, kp=0, ids=0, toks=0, ws=0) == K.KPOOL_OK
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(K, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(K, "_lib", None)
