@@ -242,12 +242,195 @@ def reference_arm(args, wl, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def rows_config(wl: W.RowsWorkload, world: int) -> dict:
+    return {"workload": wl.name, "key_seqlens": list(wl.seqlens) if len(set(wl.seqlens)) > 1 else
+            f"{len(wl.seqlens)} x {wl.seqlens[0]}", "rows": wl.num_rows, "heads": wl.heads,
+            "head_dim": wl.head_dim, "kpool": wl.kpool, "index_topk": wl.index_topk, "budget": wl.budget,
+            "scale": wl.scale, "inputs": "k, q bf16 N(0,1), w fp32 U(0,1), seeded (CUDA Philox)",
+            "l2": "pooled keys of all rows' sequences (%.0f MiB) exceed L2" % (
+                wl.total_tokens // wl.kpool * wl.head_dim * 2 / 2**20),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+ROWS_METRIC = "KPool decode selection: scored pairs/s (rows against a pooled-key cache)"
+
+
+def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
+    """Decode / short-query path: kpool_select_rows against a resident pooled-key cache."""
+    if args.impl == "reference":
+        if rank == 0:
+            from oracle import oracle
+            from tests import parity
+            oracle.build()
+            inp = W.generate_rows(wl, "cuda" if torch.cuda.is_available() else "cpu")
+            cu = inp["cu_seqlens"].cpu().numpy()
+            kp = oracle.pool(parity.bits(inp["k"]), wl.dtype, cu, wl.kpool)
+            qb, wb = parity.bits(inp["q"]), inp["w"].cpu().numpy()
+            rows = np.array(wl.global_rows(), dtype=np.int64)
+            times = []
+            for i in range(args.warmup + args.steps):
+                t0 = time.perf_counter()
+                oracle.select(qb, wb, kp, cu, rows, wl.dtype, wl.kpool, wl.index_topk, wl.scale)
+                if i >= args.warmup:
+                    times.append(time.perf_counter() - t0)
+            v = wl.scored_pairs() / statistics.median(times)
+            print(json.dumps({"impl": "reference", "metric": ROWS_METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                              "config": rows_config(wl, world),
+                              "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                                               "sample": f"all {wl.num_rows} rows, pooling excluded"},
+                              "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                  flush=True)
+        return
+    kbuild.build()
+    K.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    inp = W.generate_rows(wl, dev)
+    kp = K.kpool_pool_keys(inp["k"], inp["cu_seqlens"], wl.kpool)  # the cache exists before decoding
+    R, B, Wd = wl.num_rows, wl.budget, wl.width
+    ids = torch.empty((R, B), dtype=torch.int32, device=dev)
+    toks = torch.empty((R, Wd), dtype=torch.int32, device=dev)
+    ws = K.new_rows_workspace(R, wl.total_tokens, wl.num_seqs, wl.kpool, wl.index_topk, dev)
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for evs in step_events:
+        for e in evs:
+            e.record(stream)
+
+    def step(ev=None, q=inp["q"], w=inp["w"], rs=inp["row_seq"], rp=inp["row_pos"]):
+        K.kpool_select_rows(q, w, rs, rp, kp, inp["cu_seqlens"], wl.total_tokens, wl.kpool, wl.index_topk,
+                            wl.scale, out_pool_ids=ids, out_token_ids=toks, workspace=ws, stream=stream,
+                            stage_events=ev)
+
+    for _ in range(args.warmup):
+        step(step_events[0])
+    torch.cuda.synchronize()
+    if K.kpool_last_device_error(ws) != K.KPOOL_OK:
+        raise K.KpoolError(K.kpool_last_device_error(ws), "device")
+    # an L2-sized write between steps so every step reads the cache from HBM
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    per_step = []
+    for s_i in range(args.steps):
+        flush.fill_(s_i & 0xFF)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step(step_events[s_i])
+        b.record(stream)
+        per_step.append((a, b))
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    ms = statistics.median([a.elapsed_time(b) for a, b in per_step])
+    # the same step captured once in a CUDA graph and replayed (what a decode loop would do)
+    graph_ms = None
+    try:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(graph, stream=gs):
+                K.kpool_select_rows(inp["q"], inp["w"], inp["row_seq"], inp["row_pos"], kp, inp["cu_seqlens"],
+                                    wl.total_tokens, wl.kpool, wl.index_topk, wl.scale, out_pool_ids=ids,
+                                    out_token_ids=toks, workspace=ws, stream=gs)
+        stream.wait_stream(gs)
+        g_t = []
+        for s_i in range(args.warmup + args.steps):
+            flush.fill_(s_i & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            g_t.append((a, b))
+        torch.cuda.synchronize()
+        graph_ms = statistics.median([a.elapsed_time(b) for a, b in g_t[args.warmup:]])
+    except RuntimeError as ex:  # graph capture unavailable: report the eager number only
+        print(f"graph capture skipped: {ex}", file=sys.stderr)
+    ms_step = max_over_ranks(ms, world)
+    k_ms = [statistics.median([evs[i].elapsed_time(evs[i + 1]) for evs in step_events]) for i in range(3)]
+    pairs = wl.scored_pairs()
+    value = world * pairs / (ms_step / 1e3)
+    # e2e: the rows' inputs come from pinned host memory, the selection goes back to it
+    h = {k: torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True) for k in ("q", "w", "row_seq", "row_pos")}
+    for k2 in h:
+        h[k2].copy_(inp[k2])
+    d = {k2: torch.empty_like(inp[k2]) for k2 in h}
+    h_ids = torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True)
+    h_toks = torch.empty(toks.shape, dtype=toks.dtype, pin_memory=True)
+    bi = sum(v.numel() * v.element_size() for v in h.values())
+    bo = h_ids.numel() * 4 + h_toks.numel() * 4
+    e2e_t = []
+    for _ in range(args.warmup + args.steps):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k2 in d:
+            d[k2].copy_(h[k2], non_blocking=True)
+        step(None, d["q"], d["w"], d["row_seq"], d["row_pos"])
+        h_ids.copy_(ids, non_blocking=True)
+        h_toks.copy_(toks, non_blocking=True)
+        b.record(stream)
+        e2e_t.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.median([a.elapsed_time(b) for a, b in e2e_t[args.warmup:]]), world)
+    peaks = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    H, dd = wl.heads, wl.head_dim
+    score_bytes = pairs * dd * 2 + R * H * dd * 2 + R * H * 4 + pairs * 4  # pooled keys, q, w in; scores out
+    achieved = score_bytes / (k_ms[1] / 1e3) / 1e9
+    line = {
+        "metric": ROWS_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": rows_config(wl, world),
+        "us_per_decode_step": 1e3 * ms_step,
+        "us_per_decode_step_graph": None if graph_ms is None else 1e3 * graph_ms,
+        "kernel_ms": {"plan": k_ms[0], "score": k_ms[1], "select": k_ms[2]},
+        "roofline": {"kernel": "rows_score_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_kind": f"HBM copy, {peaks['_source']}", "algorithmic_bytes_per_launch": score_bytes},
+        "clocks": clock_info, "gpu_launches": 4 * args.steps,
+        "e2e": {"value": world * pairs / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
+    }
+    if rank == 0 and not args.no_cpu:
+        from oracle import oracle
+        from tests import parity
+        cu = inp["cu_seqlens"].cpu().numpy()
+        kpo = oracle.pool(parity.bits(inp["k"]), wl.dtype, cu, wl.kpool)
+        rows = np.array(wl.global_rows(), dtype=np.int64)
+        t0 = time.perf_counter()
+        ref = oracle.select(parity.bits(inp["q"]), inp["w"].cpu().numpy(), kpo, cu, rows, wl.dtype, wl.kpool,
+                            wl.index_topk, wl.scale)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": pairs / dt, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                                "sample": f"all {R} rows ({pairs:.3e} pairs, {dt:.2f} s, pooling excluded)"}
+        ok = True
+        try:
+            ref["kp"], ref["rows"] = kpo, rows
+            parity.compare_float({"cu_seqlens": inp["cu_seqlens"]}, wl, ref, ids.cpu().numpy(), None,
+                                 toks.cpu().numpy(), q_rows=inp["q"], w_rows=inp["w"])
+        except AssertionError as ex:
+            ok = False
+            line["parity_sample_error"] = str(ex)[:200]
+        line["parity_sample"] = {"rows": R, "ok": ok}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="pages_512k", choices=sorted(W.BY_NAME))
+    ap.add_argument("--workload", default="pages_512k", choices=sorted(W.BY_NAME) + sorted(W.ROWS_BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample-pairs", type=float, default=4.0e7,
                     help="eligible pairs in the CPU oracle's timed row sample")
@@ -257,8 +440,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    wl = W.BY_NAME[args.workload]
     world, rank, local = dist_setup()
+    if args.workload in W.ROWS_BY_NAME:
+        rows_bench(args, W.ROWS_BY_NAME[args.workload], world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    wl = W.BY_NAME[args.workload]
     if args.impl == "reference":
         reference_arm(args, wl, world, rank)
         if world > 1:

@@ -175,6 +175,19 @@ kpool_status kpool_select_rows(const void* q, const float* w, const int32_t* row
                                kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
                                int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
                                void* workspace, size_t workspace_bytes, void* stream);
+/*
+ * kpool_select_rows with options (NULL = defaults). score_kernel must be
+ * KPOOL_SCORE_AUTO; max_ctas > 0 caps the score kernel's grid; stage_events, when
+ * not NULL, holds 4 cudaEvent_t recorded on `stream` before the planning kernel
+ * and after the planning, score and select kernels.
+ */
+kpool_status kpool_select_rows_ex(const void* q, const float* w, const int32_t* row_seq, const int32_t* row_pos,
+                                  int32_t num_rows, const void* pooled_keys, const int32_t* cu_seqlens,
+                                  int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                                  kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                                  int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                                  void* workspace, size_t workspace_bytes, void* stream,
+                                  const kpool_options* options);
 
 /*
  * Synchronises `stream`, then reads the device error word the last call on this

@@ -235,6 +235,23 @@ kpool_status kpool_select_rows(const void* q, const float* w, const int32_t* row
                                kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
                                int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
                                void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  return kpool_select_rows_ex(q, w, row_seq, row_pos, num_rows, pooled_keys, cu_seqlens, num_seqs, total_tokens,
+                              heads, head_dim, dtype, kpool, index_topk, scale, out_pool_ids, out_token_ids,
+                              out_pool_scores, workspace, workspace_bytes, stream_ptr, nullptr);
+}
+
+kpool_status kpool_select_rows_ex(const void* q, const float* w, const int32_t* row_seq, const int32_t* row_pos,
+                                  int32_t num_rows, const void* pooled_keys, const int32_t* cu_seqlens,
+                                  int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                                  kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                                  int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                                  void* workspace, size_t workspace_bytes, void* stream_ptr,
+                                  const kpool_options* options) {
+  kpool_options opt{};
+  if (options) opt = *options;
+  for (int i = 0; i < 4; ++i)
+    if (opt.reserved[i] != 0) return KPOOL_ERR_INVALID_ARG;
+  if (opt.score_kernel != KPOOL_SCORE_AUTO || opt.max_ctas < 0) return KPOOL_ERR_INVALID_ARG;
   kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
   if (st != KPOOL_OK) return st;
   if (num_rows < 0 || heads < 1 || index_topk < 0 || index_topk % kpool != 0 || !isfinite(scale))
@@ -254,9 +271,11 @@ kpool_status kpool_select_rows(const void* q, const float* w, const int32_t* row
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < L.total) return KPOOL_ERR_WORKSPACE;
   int sms = 0;
   if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
+  if (opt.max_ctas > 0 && opt.max_ctas < sms) sms = opt.max_ctas;
   if (!cuda_ok(launch_select_rows(q, w, row_seq, row_pos, num_rows, pooled_keys, cu_seqlens, num_seqs,
                                   total_tokens, kpool, budget, scale, out_pool_ids, out_pool_scores, out_token_ids,
-                                  static_cast<char*>(workspace), L, sms, static_cast<cudaStream_t>(stream_ptr))))
+                                  static_cast<char*>(workspace), L, sms, static_cast<cudaStream_t>(stream_ptr),
+                                  opt.stage_events)))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
 }

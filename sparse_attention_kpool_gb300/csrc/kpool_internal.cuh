@@ -127,7 +127,7 @@ cudaError_t launch_expand(const int32_t* pool_ids, const int32_t* cu, int32_t S,
 // Selection for explicit query rows against an existing pooled-key cache
 // (kpool_rows.cu): workspace layout, shape support and the R0-R2 launches.
 struct RowsLayout {
-  size_t header, pool_off, info, unit_off, scores, total;
+  size_t header, pool_off, info, unit_off, hist, cand_cnt, tie_cnt, cleared_bytes, cand, ties, scores, total;
   int64_t stride;  // floats per row of the score buffer (>= T / kpool, multiple of 4)
 };
 RowsLayout rows_layout(int32_t R, int64_t T, int32_t S, int32_t kpool);
@@ -136,7 +136,7 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
                                int32_t R, const void* kp, const int32_t* cu, int32_t S, int64_t T, int32_t kpool,
                                int32_t budget, float scale, int32_t* out_ids, float* out_scores,
                                int32_t* out_tokens, char* ws, const RowsLayout& L, int num_sms,
-                               cudaStream_t stream);
+                               cudaStream_t stream, void* const* stage_events);
 
 // Bounded-wait self test.
 cudaError_t launch_wait_selftest(char* ws, int64_t spin_limit, cudaStream_t stream);

@@ -12,11 +12,16 @@
 // over many CTAs and keeps the [rows, pools] scores (a few MiB, L2-resident):
 //   R0 rows_plan_kernel   (1 CTA)   checks cu_seqlens and the rows, pool offsets,
 //                                   per-row eligible counts and the work units
-//   R1 rows_score_kernel  (grid)    one unit = up to 1024 pools of one row; bf16
+//   R1 rows_score_kernel  (grid)    each CTA a contiguous run of 128-pool units; bf16
 //                                   mma.sync tensor-core products, relu / weight /
 //                                   head sum in registers, fp32 scores out
-//   R2 rows_select_kernel (1 CTA / row) exact top-budget by an MSD radix search
-//                                   on the scores, ties to the smaller pool, a
+//   R2 rows_collect_kernel (grid)   from a per-row histogram of the scores' top 12
+//                                   bits (built by R1) finds the bin holding the
+//                                   budget-th score, then gathers every pool above
+//                                   that bin and the pools inside it
+//   R3 rows_select_kernel (1 CTA / row) exact top-budget among the gathered pools
+//                                   (ties to the smaller pool; a full MSD radix
+//                                   search over the row when the bin overflows), a
 //                                   register bitonic sort, ids / scores / tokens
 // R1 streams the pooled keys once per row (HBM-bound: 256 B per pool); the
 // contraction per pool is 32 heads x 128 channels, small enough that the
@@ -34,10 +39,17 @@ namespace {
 
 constexpr int kRowsHeads = 32;
 constexpr int kRowsDim = 128;
-constexpr int kUnitPools = 1024;       // pools per work unit of R1
-constexpr int kScoreWarps = 8;         // R1: 8 warps x 128 pools = one unit
-constexpr int kSelectThreads = 512;    // R2
-constexpr int kRowsMaxBudget = 512;    // R2 sorts at most 512 keys in one warp
+constexpr int kUnitPools = 128;        // pools per work unit of R1 (the split granularity)
+constexpr int kScoreWarps = 8;         // R1: 8 warps x 16 pools per round
+constexpr int kSelectThreads = 256;    // R3
+constexpr int kRowsMaxBudget = 512;    // R3 sorts at most 512 keys in one warp
+constexpr int kHistBits = 12;          // histogram of score_order_bits >> (32 - kHistBits)
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kTieCap = 4096;          // pools of the threshold bin R3 can finish in shared memory
+constexpr int kCollectPools = 2048;    // R2: pools per CTA and round
+constexpr int kCollectTies = 2048;     // R2: threshold-bin pools one round can hold
+constexpr int kCollectCtasPerRow = 64; // R2: grid width; CTAs loop over a row's slices
+constexpr int kCollectThreads = 256;
 
 struct RowInfo {
   int32_t pool_base;  // global pooled-key row of the sequence's pool 0
@@ -161,14 +173,20 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 __global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
     const uint4* __restrict__ q, const float* __restrict__ w, const uint4* __restrict__ kp,
     const RowInfo* __restrict__ info, const int32_t* __restrict__ unit_off, const WorkspaceHeader* hdr, int R,
-    float scale, float* __restrict__ scores, int64_t stride) {
+    float scale, float* __restrict__ scores, int64_t stride, uint32_t* __restrict__ hist) {
+  __shared__ uint32_t s_hist[kHistBins];  // this unit's histogram, flushed to the row's at the end
+  __shared__ uint4 s_q[16][32];           // the row's query fragments (see below)
   const int n_units = hdr->n_items;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const float abs_scale = fabsf(scale);
   const bool neg = scale < 0.0f;
   constexpr int kVecPerRow = kRowsDim / 8;  // 16-byte vectors per pooled key / query head
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  // this CTA's share: a contiguous run of units, i.e. one or a few contiguous pool
+  // ranges ("segments") of consecutive rows
+  const int u_first = int(int64_t(n_units) * blockIdx.x / gridDim.x);
+  const int u_last = int(int64_t(n_units) * (blockIdx.x + 1) / gridDim.x);
+  for (int u = u_first; u < u_last;) {
     // row of unit u: the last r with unit_off[r] <= u
     int lo = 0, hi = R - 1;
     while (lo < hi) {
@@ -177,14 +195,19 @@ __global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
     }
     const int r = lo;
     const RowInfo ri = info[r];
+    const int seg_end = min(u_last, __ldg(unit_off + r + 1));
     const int p_begin = (u - unit_off[r]) * kUnitPools;
     const int e = ri.e;
-    // query fragments of all 32 heads: qf[n][m] holds channels 32m + 8c .. + 7 of head g + 8n
-    uint4 qf[4][4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-      for (int m = 0; m < 4; ++m) qf[n][m] = __ldg(q + (int64_t(r) * kRowsHeads + g + 8 * n) * kVecPerRow + 4 * m + c);
+    const int p_end = min(e, (seg_end - unit_off[r]) * kUnitPools);
+    u = seg_end;
+    // query fragments of all 32 heads, one copy per lane slot in shared memory so the
+    // registers stay free for a second set of pooled-key loads in flight:
+    // s_q[n * 4 + m][lane] holds channels 32m + 8c .. + 7 of head g + 8n
+    __syncthreads();  // the previous unit's fragments are no longer read
+    for (int i = threadIdx.x; i < 16 * 32; i += blockDim.x) {
+      const int f = i >> 5, l = i & 31, n = f >> 2, m = f & 3;
+      s_q[f][l] = __ldg(q + (int64_t(r) * kRowsHeads + (l >> 2) + 8 * n) * kVecPerRow + 4 * m + (l & 3));
+    }
     // this thread's accumulator columns are heads 8n + 2c and 8n + 2c + 1
     float wt[4][2];
 #pragma unroll
@@ -193,16 +216,24 @@ __global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
       wt[n][1] = __ldg(w + int64_t(r) * kRowsHeads + 8 * n + 2 * c + 1) * abs_scale;
     }
     float* out = scores + int64_t(r) * stride;
-    for (int p0 = p_begin + warp * 16; p0 < min(e, p_begin + kUnitPools); p0 += kScoreWarps * 16) {
-      // pooled keys of pools p0 + g and p0 + g + 8 (clamped to an eligible pool; the
-      // scores of clamped rows are not stored)
-      const int pa = min(p0 + g, e - 1), pb = min(p0 + g + 8, e - 1);
-      uint4 ka[4], kb[4];
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) s_hist[i] = 0;
+    __syncthreads();
+    // pooled keys of pools p + g and p + g + 8, clamped to an eligible pool (the scores
+    // of clamped rows are not stored); the next 16 pools load while these are scored
+    auto load_keys = [&](int p, uint4 (&ka)[4], uint4 (&kb)[4]) {
+      const int pa = min(p + g, e - 1), pb = min(p + g + 8, e - 1);
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         ka[m] = __ldg(kp + int64_t(ri.pool_base + pa) * kVecPerRow + 4 * m + c);
         kb[m] = __ldg(kp + int64_t(ri.pool_base + pb) * kVecPerRow + 4 * m + c);
       }
+    };
+    uint4 ka[4], kb[4], na[4], nb[4];
+    int p0 = p_begin + warp * 16;
+    if (p0 < p_end) load_keys(p0, ka, kb);
+    for (; p0 < p_end; p0 += kScoreWarps * 16) {
+      const int pn = p0 + kScoreWarps * 16;
+      if (pn < p_end) load_keys(pn, na, nb);
       float acc[4][4];
 #pragma unroll
       for (int n = 0; n < 4; ++n)
@@ -214,9 +245,15 @@ __global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
         const uint32_t a_hi[4] = {ka[m].z, kb[m].z, ka[m].w, kb[m].w};  // k-step 2m + 1
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          mma_bf16_16816(acc[n], a_lo, qf[n][m].x, qf[n][m].y);
-          mma_bf16_16816(acc[n], a_hi, qf[n][m].z, qf[n][m].w);
+          const uint4 qf = s_q[n * 4 + m][lane];
+          mma_bf16_16816(acc[n], a_lo, qf.x, qf.y);
+          mma_bf16_16816(acc[n], a_hi, qf.z, qf.w);
         }
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        ka[m] = na[m];
+        kb[m] = nb[m];
       }
       // acc[n][0..1]: pool g, heads 8n + 2c, +1; acc[n][2..3]: pool g + 8
       float sa = 0.0f, sb = 0.0f;
@@ -232,9 +269,118 @@ __global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
       sa += __shfl_xor_sync(0xffffffffu, sa, 2);
       sb += __shfl_xor_sync(0xffffffffu, sb, 1);
       sb += __shfl_xor_sync(0xffffffffu, sb, 2);
-      if (c == 0 && p0 + g < e) out[p0 + g] = sa;
-      if (c == 1 && p0 + g + 8 < e) out[p0 + g + 8] = sb;
+      const int pm = c == 0 ? p0 + g : p0 + g + 8;
+      const float sm = c == 0 ? sa : sb;
+      const bool has = c < 2 && pm < e;
+      if (has) out[pm] = sm;
+      // histogram of the top bits, one shared atomic per distinct bin in the warp
+      const uint32_t bin = score_order_bits(sm) >> (32 - kHistBits);
+      const unsigned act = __ballot_sync(0xffffffffu, has);
+      if (has) {
+        const unsigned peers = __match_any_sync(act, bin);
+        if ((__ffs(peers) - 1) == lane) atomicAdd(s_hist + bin, uint32_t(__popc(peers)));
+      }
     }
+    __syncthreads();
+    uint32_t* h = hist + int64_t(r) * kHistBins;
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
+      const uint32_t v = s_hist[i];
+      if (v) atomicAdd(h + i, v);
+    }
+    __syncthreads();
+  }
+}
+
+// --------------------------------------------------------------- R2 collect
+//
+// Bin b of a row's histogram counts the pools whose score_order_bits has top
+// bits b. Scanning the bins from the top, the threshold bin is the one where
+// the running count first reaches the budget: every pool in a higher bin is
+// chosen (fewer than budget of them), the rest of the budget comes from the
+// threshold bin.
+__device__ __forceinline__ void threshold_bin(const uint32_t* __restrict__ h, int budget, int* s_warp,
+                                              int* out_bin, int* out_above) {
+  constexpr int kPer = kHistBins / kCollectThreads;  // bins per thread, descending
+  const int tid = threadIdx.x;
+  uint32_t cnt[kPer];
+  int tot = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    cnt[i] = h[kHistBins - 1 - (kPer * tid + i)];
+    tot += int(cnt[i]);
+  }
+  int all;
+  const int before = block_exclusive_scan(tot, &all, s_warp);
+  if (before < budget && before + tot >= budget) {
+    int run = before, i = 0;
+    while (i < kPer - 1 && run + int(cnt[i]) < budget) run += int(cnt[i++]);
+    *out_bin = kHistBins - 1 - (kPer * tid + i);
+    *out_above = run;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kCollectThreads) rows_collect_kernel(
+    const float* __restrict__ scores, int64_t stride, const RowInfo* __restrict__ info, const WorkspaceHeader* hdr,
+    int budget, const uint32_t* __restrict__ hist, int32_t* cand_cnt, uint64_t* __restrict__ cand,
+    int32_t* tie_cnt, uint64_t* __restrict__ ties) {
+  __shared__ int s_warp[32];
+  __shared__ int s_bin, s_above, s_na, s_nt, s_base_a, s_base_t;
+  __shared__ uint64_t s_a[kRowsMaxBudget];
+  __shared__ uint64_t s_t[kCollectTies];
+  const int r = blockIdx.y;
+  if (hdr->n_levels == 0) return;
+  const RowInfo ri = info[r];
+  const int e = ri.e;
+  if (budget <= 0 || e <= budget || int(blockIdx.x) * kCollectPools >= e) return;  // includes invalid rows
+  threshold_bin(hist + int64_t(r) * kHistBins, budget, s_warp, &s_bin, &s_above);
+  const uint32_t thr = uint32_t(s_bin);
+  const float* row = scores + int64_t(r) * stride;
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int p_lo = blockIdx.x * kCollectPools; p_lo < e; p_lo += gridDim.x * kCollectPools) {
+    if (threadIdx.x == 0) {
+      s_na = 0;
+      s_nt = 0;
+    }
+    __syncthreads();
+    const int p_hi = min(e, p_lo + kCollectPools);
+    // gather this slice's pools above / inside the threshold bin in shared memory (whole
+    // warps iterate together for the warp votes)
+    for (int p = p_lo + threadIdx.x; p < p_lo + ((p_hi - p_lo + 31) & ~31); p += kCollectThreads) {
+      float s = 0.0f;
+      uint32_t bin = 0;
+      const bool in = p < p_hi;
+      if (in) {
+        s = row[p];
+        bin = score_order_bits(s) >> (32 - kHistBits);
+      }
+      const bool above = in && bin > thr, tie = in && bin == thr;
+      const unsigned ma = __ballot_sync(0xffffffffu, above), mt = __ballot_sync(0xffffffffu, tie);
+      int base_a = 0, base_t = 0;
+      if (lane == 0) {
+        if (ma) base_a = atomicAdd(&s_na, __popc(ma));
+        if (mt) base_t = atomicAdd(&s_nt, __popc(mt));
+      }
+      base_a = __shfl_sync(0xffffffffu, base_a, 0) + __popc(ma & lt);
+      base_t = __shfl_sync(0xffffffffu, base_t, 0) + __popc(mt & lt);
+      if (above && base_a < kRowsMaxBudget) s_a[base_a] = make_key(s, uint32_t(p));
+      if (tie && base_t < kCollectTies) s_t[base_t] = make_key(s, uint32_t(p));
+    }
+    __syncthreads();
+    // one reservation per slice in the row's gather lists; a slice with more ties than
+    // it can hold reserves past the list's end, which sends the row to the full search
+    if (threadIdx.x == 0) {
+      s_base_a = s_na ? atomicAdd(cand_cnt + r, s_na) : 0;
+      s_base_t = s_nt ? atomicAdd(tie_cnt + r, s_nt <= kCollectTies ? s_nt : kTieCap + 1) : 0;
+    }
+    __syncthreads();
+    const int na = min(s_na, kRowsMaxBudget), nt = min(s_nt, kCollectTies);
+    for (int i = threadIdx.x; i < na; i += kCollectThreads)
+      if (s_base_a + i < kRowsMaxBudget) cand[int64_t(r) * kRowsMaxBudget + s_base_a + i] = s_a[i];
+    for (int i = threadIdx.x; i < nt; i += kCollectThreads)
+      if (s_base_t + i < kTieCap) ties[int64_t(r) * kTieCap + s_base_t + i] = s_t[i];
+    __syncthreads();
   }
 }
 
@@ -248,8 +394,11 @@ __global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
 // the smallest indices until the budget is full.
 __global__ void __launch_bounds__(kSelectThreads) rows_select_kernel(
     const float* __restrict__ scores, int64_t stride, const RowInfo* __restrict__ info,
-    const WorkspaceHeader* hdr, int kpool, int budget, int32_t* __restrict__ out_ids,
-    float* __restrict__ out_scores, int32_t* __restrict__ out_tokens) {
+    const WorkspaceHeader* hdr, int kpool, int budget, const int32_t* __restrict__ cand_cnt,
+    const uint64_t* __restrict__ cand, const int32_t* __restrict__ tie_cnt, const uint64_t* __restrict__ ties,
+    int32_t* __restrict__ out_ids, float* __restrict__ out_scores, int32_t* __restrict__ out_tokens) {
+  __shared__ uint64_t s_ties[kTieCap];
+  __shared__ SelectScratch s_sel;
   __shared__ uint32_t s_hist[256];
   __shared__ int s_warp[32];
   __shared__ uint32_t s_digit, s_above;
@@ -275,9 +424,25 @@ __global__ void __launch_bounds__(kSelectThreads) rows_select_kernel(
   for (int j = tid; j < kRowsMaxBudget; j += kSelectThreads) s_keys[j] = 0ull;
   __syncthreads();
 
+  const int n_above = e > budget ? cand_cnt[r] : 0, n_tie = e > budget ? tie_cnt[r] : 0;
   if (e <= budget) {
     for (int p = tid; p < e; p += kSelectThreads) s_keys[p] = make_key(row[p], uint32_t(p));
+  } else if (budget > 0 && n_tie <= kTieCap) {
+    // R2 gathered the n_above pools above the threshold bin and the n_tie pools in it:
+    // keep the first, and the top budget - n_above of the second by full key
+    for (int j = tid; j < n_above; j += kSelectThreads) s_keys[j] = cand[int64_t(r) * kRowsMaxBudget + j];
+    for (int j = tid; j < n_tie; j += kSelectThreads) s_ties[j] = ties[int64_t(r) * kTieCap + j];
+    __syncthreads();
+    const int need = budget - n_above;
+    if (n_tie > need) {
+      uint64_t edge;
+      block_select_compact<kTieCap / kSelectThreads, kSelectThreads / 32>(s_ties, n_tie, need, 0, tid, 1, &s_sel,
+                                                                         &edge);
+    }
+    for (int j = tid; j < need; j += kSelectThreads) s_keys[n_above + j] = s_ties[j];
   } else if (budget > 0) {
+    // the threshold bin holds more pools than fit in shared memory (long runs of
+    // equal scores): search the row itself
     // MSD radix search for v = the budget-th largest score_order_bits value
     uint32_t prefix = 0;
     int above = 0;  // pools whose bits exceed every value still in the bin
@@ -402,11 +567,20 @@ RowsLayout rows_layout(int32_t R, int64_t T, int32_t S, int32_t kpool) {
   int64_t stride = T / kpool;
   stride = ((stride > 0 ? stride : 1) + 3) & ~int64_t(3);
   L.stride = stride;
+  const size_t nr = size_t(R > 0 ? R : 1);
   size_t off = 0;
   L.header = off;   off = align256(off + sizeof(WorkspaceHeader));
   L.pool_off = off; off = align256(off + sizeof(int32_t) * size_t(S + 1));
-  L.info = off;     off = align256(off + sizeof(RowInfo) * size_t(R > 0 ? R : 1));
+  L.info = off;     off = align256(off + sizeof(RowInfo) * nr);
   L.unit_off = off; off = align256(off + sizeof(int32_t) * size_t(R + 1));
+  // cleared before every call: histograms, then the two gather counters per row
+  L.hist = off;     off += sizeof(uint32_t) * size_t(kHistBins) * nr;
+  L.cand_cnt = off; off += sizeof(int32_t) * nr;
+  L.tie_cnt = off;  off += sizeof(int32_t) * nr;
+  L.cleared_bytes = off - L.hist;
+  off = align256(off);
+  L.cand = off;     off = align256(off + sizeof(uint64_t) * size_t(kRowsMaxBudget) * nr);
+  L.ties = off;     off = align256(off + sizeof(uint64_t) * size_t(kTieCap) * nr);
   L.scores = off;   off = align256(off + sizeof(float) * size_t(R) * size_t(stride));
   L.total = off;
   return L;
@@ -420,26 +594,48 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
                                int32_t R, const void* kp, const int32_t* cu, int32_t S, int64_t T, int32_t kpool,
                                int32_t budget, float scale, int32_t* out_ids, float* out_scores,
                                int32_t* out_tokens, char* ws, const RowsLayout& L, int num_sms,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, void* const* stage_events) {
   WorkspaceHeader* hdr = reinterpret_cast<WorkspaceHeader*>(ws + L.header);
   int32_t* pool_off = reinterpret_cast<int32_t*>(ws + L.pool_off);
   RowInfo* info = reinterpret_cast<RowInfo*>(ws + L.info);
   int32_t* unit_off = reinterpret_cast<int32_t*>(ws + L.unit_off);
   float* scores = reinterpret_cast<float*>(ws + L.scores);
-  rows_plan_kernel<<<1, 1024, 0, stream>>>(cu, S, T, row_seq, row_pos, R, kpool, hdr, pool_off, info, unit_off);
-  cudaError_t e = cudaGetLastError();
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  int32_t* cand_cnt = reinterpret_cast<int32_t*>(ws + L.cand_cnt);
+  int32_t* tie_cnt = reinterpret_cast<int32_t*>(ws + L.tie_cnt);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(ws + L.cand);
+  uint64_t* ties = reinterpret_cast<uint64_t*>(ws + L.ties);
+  auto mark = [&](int i) {
+    return stage_events == nullptr ? cudaSuccess
+                                   : cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), stream);
+  };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.hist, 0, L.cleared_bytes, stream);
   if (e != cudaSuccess) return e;
-  // units: at most R * ceil(max pools / kUnitPools); a few waves of 2 CTAs per SM
+  rows_plan_kernel<<<1, 1024, 0, stream>>>(cu, S, T, row_seq, row_pos, R, kpool, hdr, pool_off, info, unit_off);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = mark(1);
+  if (e != cudaSuccess) return e;
+  // units: at most R * ceil(max pools / kUnitPools); one wave of 2 CTAs per SM splits them
   const int64_t max_units = int64_t(R) * ((L.stride + kUnitPools - 1) / kUnitPools);
-  const int grid = int(max_units < int64_t(4) * num_sms ? (max_units > 0 ? max_units : 1) : int64_t(4) * num_sms);
+  const int grid = int(max_units < int64_t(2) * num_sms ? (max_units > 0 ? max_units : 1) : int64_t(2) * num_sms);
   rows_score_kernel<<<grid, kScoreWarps * 32, 0, stream>>>(static_cast<const uint4*>(q), w,
                                                              static_cast<const uint4*>(kp), info, unit_off, hdr,
-                                                             R, scale, scores, L.stride);
+                                                             R, scale, scores, L.stride, hist);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = mark(2);
+  if (e != cudaSuccess) return e;
+  const int64_t slices = (L.stride + kCollectPools - 1) / kCollectPools;
+  const dim3 cgrid(unsigned(slices < kCollectCtasPerRow ? slices : kCollectCtasPerRow), unsigned(R));
+  rows_collect_kernel<<<cgrid, kCollectThreads, 0, stream>>>(scores, L.stride, info, hdr, budget, hist, cand_cnt,
+                                                              cand, tie_cnt, ties);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  rows_select_kernel<<<R, kSelectThreads, 0, stream>>>(scores, L.stride, info, hdr, kpool, budget, out_ids,
-                                                       out_scores, out_tokens);
-  return cudaGetLastError();
+  rows_select_kernel<<<R, kSelectThreads, 0, stream>>>(scores, L.stride, info, hdr, kpool, budget, cand_cnt, cand,
+                                                       tie_cnt, ties, out_ids, out_scores, out_tokens);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = mark(3);
+  return e;
 }
 
 }  // namespace kpool

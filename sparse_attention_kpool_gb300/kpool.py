@@ -38,7 +38,7 @@ KPOOL_SCORE_SIMT = 2
 EXPORTED = (
     "kpool_workspace_bytes", "kpool_select", "kpool_select_ex", "kpool_pool_keys", "kpool_expand",
     "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string", "kpool_last_cuda_error",
-    "kpool_select_static_scratch", "kpool_rows_workspace_bytes", "kpool_select_rows",
+    "kpool_select_static_scratch", "kpool_rows_workspace_bytes", "kpool_select_rows", "kpool_select_rows_ex",
 )
 KPOOL_STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -100,6 +100,8 @@ def load() -> ctypes.CDLL:
         lib.kpool_select_rows.argtypes = [P, P, P, P, i32, P, P, i32, i64, i32, i32, i32, i32, i32, f32, P, P, P,
                                           P, sz, P]
         lib.kpool_select_rows.restype = i32
+        lib.kpool_select_rows_ex.argtypes = lib.kpool_select_rows.argtypes + [ctypes.POINTER(kpool_options)]
+        lib.kpool_select_rows_ex.restype = i32
         _lib = lib
         return lib
 
@@ -279,13 +281,16 @@ def new_rows_workspace(num_rows: int, total_tokens: int, num_seqs: int, kpool: i
 def kpool_select_rows(q: torch.Tensor, w: torch.Tensor, row_seq: torch.Tensor, row_pos: torch.Tensor,
                       pooled_keys: torch.Tensor, cu_seqlens: torch.Tensor, total_tokens: int, kpool: int,
                       index_topk: int, scale: float, out_pool_ids=None, out_token_ids=None, out_pool_scores=None,
-                      return_scores: bool = False, workspace=None, stream=None):
+                      return_scores: bool = False, workspace=None, stream=None, max_ctas: int = 0,
+                      stage_events=None):
     """Selection for explicit query rows against an existing pooled-key cache (decode).
 
     q [R,H,d] bf16, w [R,H] fp32, row_seq / row_pos [R] int32 (sequence and local position of
     each row), pooled_keys [>= P, d] as kpool_pool_keys returns them for cu_seqlens [S+1]
     (the key batch of total_tokens tokens) -> (pool_ids [R,B], token_ids [R, index_topk+kpool],
-    pool_scores [R,B] or None)."""
+    pool_scores [R,B] or None).
+
+    stage_events: optional 4 already-recorded timing events, re-recorded around the three kernels."""
     R, H, d = q.shape
     S = cu_seqlens.numel() - 1
     dt = _dtype_code(q)
@@ -304,10 +309,18 @@ def kpool_select_rows(q: torch.Tensor, w: torch.Tensor, row_seq: torch.Tensor, r
         workspace = new_rows_workspace(R, total_tokens, S, kpool, index_topk, dev)
     _check_cuda(q, w, row_seq, row_pos, pooled_keys, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores,
                 workspace)
-    st = load().kpool_select_rows(_ptr(q), _ptr(w), _ptr(row_seq), _ptr(row_pos), R, _ptr(pooled_keys),
-                                  _ptr(cu_seqlens), S, int(total_tokens), H, d, dt, kpool, index_topk, float(scale),
-                                  _ptr(out_pool_ids), _ptr(out_token_ids), _ptr(out_pool_scores), _ptr(workspace),
-                                  workspace.numel(), _stream(stream))
+    opts = kpool_options(KPOOL_SCORE_AUTO, max_ctas)
+    if stage_events is not None:
+        if len(stage_events) != 4:
+            raise ValueError("stage_events needs 4 events")
+        arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(int(e.cuda_event)) for e in stage_events])
+        if not all(arr):
+            raise ValueError("record each event once before passing it (torch creates events lazily)")
+        opts.stage_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    st = load().kpool_select_rows_ex(_ptr(q), _ptr(w), _ptr(row_seq), _ptr(row_pos), R, _ptr(pooled_keys),
+                                     _ptr(cu_seqlens), S, int(total_tokens), H, d, dt, kpool, index_topk,
+                                     float(scale), _ptr(out_pool_ids), _ptr(out_token_ids), _ptr(out_pool_scores),
+                                     _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts))
     if st != KPOOL_OK:
         raise KpoolError(st, "kpool_select_rows")
     return out_pool_ids, out_token_ids, out_pool_scores

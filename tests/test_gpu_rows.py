@@ -158,3 +158,21 @@ def test_rows_decode_262k_full_size():
     ref = _oracle_rows(wl, inp)
     parity.compare_float({"cu_seqlens": inp["cu_seqlens"]}, wl, ref, ids, sc, toks, q_rows=inp["q"],
                          w_rows=inp["w"])
+
+
+def test_rows_equal_scores_take_the_smallest_pools():
+    """All weights zero: every eligible pool scores 0, so the row keeps its budget smallest pool
+    indices. One row's threshold bin fits the gather buffer, the other's (8,191 tied pools) does
+    not and takes the full search over the row."""
+    base = W.DECODE_TIE
+    wl = W.RowsWorkload("zero_w", (40000,), ((0, 4000), (0, 32767)), 32, 128, 4, 2048, 1.0 / 16.0, "bf16",
+                        "integer", 21)
+    inp = W.generate_rows(wl, "cuda")
+    inp["w"].zero_()
+    ids, toks, sc, st = _run_rows(wl, inp)
+    assert st == K.KPOOL_OK
+    ref = _oracle_rows(wl, inp)
+    parity.assert_exact(ref, ids, toks)
+    np.testing.assert_array_equal(ids[0], np.arange(wl.budget, dtype=np.int32))
+    np.testing.assert_array_equal(ids[1], np.arange(wl.budget, dtype=np.int32))
+    assert base.budget == wl.budget
