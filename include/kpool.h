@@ -177,7 +177,7 @@ kpool_status kpool_select_rows(const void* q, const float* w, const int32_t* row
                                void* workspace, size_t workspace_bytes, void* stream);
 /*
  * kpool_select_rows with options (NULL = defaults). score_kernel must be
- * KPOOL_SCORE_AUTO; max_ctas > 0 caps the score kernel's grid; stage_events, when
+ * KPOOL_SCORE_AUTO; max_ctas > 0 caps the score kernel's grid (CTAs); stage_events, when
  * not NULL, holds 4 cudaEvent_t recorded on `stream` before the planning kernel
  * and after the planning, score and select kernels.
  */

@@ -271,11 +271,10 @@ kpool_status kpool_select_rows_ex(const void* q, const float* w, const int32_t* 
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < L.total) return KPOOL_ERR_WORKSPACE;
   int sms = 0;
   if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
-  if (opt.max_ctas > 0 && opt.max_ctas < sms) sms = opt.max_ctas;
   if (!cuda_ok(launch_select_rows(q, w, row_seq, row_pos, num_rows, pooled_keys, cu_seqlens, num_seqs,
                                   total_tokens, kpool, budget, scale, out_pool_ids, out_pool_scores, out_token_ids,
-                                  static_cast<char*>(workspace), L, sms, static_cast<cudaStream_t>(stream_ptr),
-                                  opt.stage_events)))
+                                  static_cast<char*>(workspace), L, sms, opt.max_ctas,
+                                  static_cast<cudaStream_t>(stream_ptr), opt.stage_events)))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
 }

@@ -135,7 +135,7 @@ bool select_rows_supported(kpool_dtype dtype, int32_t H, int32_t d, int32_t budg
 cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row_seq, const int32_t* row_pos,
                                int32_t R, const void* kp, const int32_t* cu, int32_t S, int64_t T, int32_t kpool,
                                int32_t budget, float scale, int32_t* out_ids, float* out_scores,
-                               int32_t* out_tokens, char* ws, const RowsLayout& L, int num_sms,
+                               int32_t* out_tokens, char* ws, const RowsLayout& L, int num_sms, int max_ctas,
                                cudaStream_t stream, void* const* stage_events);
 
 // Bounded-wait self test.

@@ -593,7 +593,7 @@ bool select_rows_supported(kpool_dtype dtype, int32_t H, int32_t d, int32_t budg
 cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row_seq, const int32_t* row_pos,
                                int32_t R, const void* kp, const int32_t* cu, int32_t S, int64_t T, int32_t kpool,
                                int32_t budget, float scale, int32_t* out_ids, float* out_scores,
-                               int32_t* out_tokens, char* ws, const RowsLayout& L, int num_sms,
+                               int32_t* out_tokens, char* ws, const RowsLayout& L, int num_sms, int max_ctas,
                                cudaStream_t stream, void* const* stage_events) {
   WorkspaceHeader* hdr = reinterpret_cast<WorkspaceHeader*>(ws + L.header);
   int32_t* pool_off = reinterpret_cast<int32_t*>(ws + L.pool_off);
@@ -618,7 +618,8 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
   if (e != cudaSuccess) return e;
   // units: at most R * ceil(max pools / kUnitPools); one wave of 2 CTAs per SM splits them
   const int64_t max_units = int64_t(R) * ((L.stride + kUnitPools - 1) / kUnitPools);
-  const int grid = int(max_units < int64_t(2) * num_sms ? (max_units > 0 ? max_units : 1) : int64_t(2) * num_sms);
+  int grid = int(max_units < int64_t(2) * num_sms ? (max_units > 0 ? max_units : 1) : int64_t(2) * num_sms);
+  if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   rows_score_kernel<<<grid, kScoreWarps * 32, 0, stream>>>(static_cast<const uint4*>(q), w,
                                                              static_cast<const uint4*>(kp), info, unit_off, hdr,
                                                              R, scale, scores, L.stride, hist);

@@ -176,3 +176,19 @@ def test_rows_equal_scores_take_the_smallest_pools():
     np.testing.assert_array_equal(ids[0], np.arange(wl.budget, dtype=np.int32))
     np.testing.assert_array_equal(ids[1], np.arange(wl.budget, dtype=np.int32))
     assert base.budget == wl.budget
+
+
+@pytest.mark.parametrize("max_ctas", [1, 3, 7, 40])
+def test_rows_any_score_grid_gives_the_same_result(max_ctas):
+    """The score kernel splits the rows' pools into contiguous runs per CTA; any split
+    (one CTA for everything, runs crossing row boundaries) gives identical output."""
+    wl = W.DECODE_SMALL
+    inp = W.generate_rows(wl, "cuda")
+    ids_ref, toks_ref, sc_ref, _ = _run_rows(wl, inp)
+    kp = K.kpool_pool_keys(inp["k"], inp["cu_seqlens"], wl.kpool)
+    ids, toks, sc = K.kpool_select_rows(inp["q"], inp["w"], inp["row_seq"], inp["row_pos"], kp, inp["cu_seqlens"],
+                                        wl.total_tokens, wl.kpool, wl.index_topk, wl.scale, return_scores=True,
+                                        max_ctas=max_ctas)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_array_equal(toks.cpu().numpy(), toks_ref)
+    np.testing.assert_array_equal(sc.cpu().numpy(), sc_ref)
