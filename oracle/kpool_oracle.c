@@ -122,6 +122,53 @@ int kpool_oracle_pool(const void* k, int dtype, const int32_t* cu_seqlens, int n
   return ORACLE_OK;
 }
 
+/* Gated pooling: a second pooling operator, a stated reading of parameters the
+   pages name without a formula. The GLM-5.3 DSA shard plan lists
+   indexer.index_kpool_compress_gate, shaped [index_head_dim, hidden] (one gate
+   score per token and key channel), and indexer.index_kpool_compress_ape,
+   shaped [kpool, index_head_dim] (one vector per position inside a pool)
+   ("spark_model/layers/glm5next_dsa/tp.rs", the indexer parameter list), and
+   the Megatron change passes "gate scores" to the fused top-k ("NVIDIA/Megatron-
+   LM pull request #8299", section "Mechanism"). Read as gated compression: per
+   pool and channel, a softmax over the pool's kpool positions of the tokens'
+   gate scores weights the keys plus their position embedding,
+       kp[p,c] = sum_j softmax_j(gate[t_j,c]) * (k[t_j,c] + ape[j,c]),
+   t_j = start + p*kpool + j. Computed in fp64 (max-subtracted softmax), then
+   rounded to fp32 and, for bf16 inputs, to bf16 (round to nearest even).
+   gate is [T, d] fp32, ape is [kpool, d] fp32. */
+int kpool_oracle_pool_gated(const void* k, int dtype, const float* gate, const float* ape,
+                            const int32_t* cu_seqlens, int num_seqs, int head_dim, int kpool,
+                            float* out_kp) {
+  if (kpool < 1 || head_dim < 1) return ORACLE_BAD_ARG;
+  int64_t out_row = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    int64_t start = cu_seqlens[b];
+    int64_t len = (int64_t)cu_seqlens[b + 1] - start;
+    int64_t n_pools = len / kpool;
+    for (int64_t p = 0; p < n_pools; ++p, ++out_row) {
+      for (int c = 0; c < head_dim; ++c) {
+        int64_t t0 = start + p * kpool;
+        double m = -INFINITY;
+        for (int j = 0; j < kpool; ++j) {
+          double g = gate[(t0 + j) * head_dim + c];
+          if (g > m) m = g;
+        }
+        double den = 0.0;
+        for (int j = 0; j < kpool; ++j) den += exp((double)gate[(t0 + j) * head_dim + c] - m);
+        double v = 0.0;
+        for (int j = 0; j < kpool; ++j) {
+          double wj = exp((double)gate[(t0 + j) * head_dim + c] - m) / den;
+          v += wj * ((double)load_elem(k, dtype, (t0 + j) * head_dim + c) + (double)ape[(int64_t)j * head_dim + c]);
+        }
+        float f = (float)v;
+        if (dtype == ORACLE_BF16) f = bf16_to_float(float_to_bf16_rne(f));
+        out_kp[out_row * head_dim + c] = f;
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* ---- step 2: score ------------------------------------------------------ */
 
 /* s = sum_h w[h] * max(0, scale * (q[h,:] . kp[:])), all in fp64.

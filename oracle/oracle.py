@@ -60,6 +60,8 @@ def open_library(path: str):
     lib.kpool_oracle_pool_offsets.restype = i32
     lib.kpool_oracle_pool.argtypes = [P, i32, P, i32, i32, i32, P]
     lib.kpool_oracle_pool.restype = i32
+    lib.kpool_oracle_pool_gated.argtypes = [P, i32, P, P, P, i32, i32, i32, P]
+    lib.kpool_oracle_pool_gated.restype = i32
     lib.kpool_oracle_score.argtypes = [P, i32, P, P, i32, i32, ctypes.c_float]
     lib.kpool_oracle_score.restype = ctypes.c_double
     lib.kpool_oracle_select.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32,
@@ -113,6 +115,26 @@ def pool(k: np.ndarray, dtype: str, cu_seqlens: np.ndarray, kpool: int, lib=None
     P = int(pool_offsets(cu, kpool, lib)[-1])
     out = np.zeros((P, d), dtype=np.float32)
     rc = _load(lib).kpool_oracle_pool(_ptr(k), DTYPES[dtype], _ptr(cu), len(cu) - 1, d, kpool, _ptr(out))
+    if rc != 0:
+        raise ValueError("invalid pooling arguments")
+    return out
+
+
+def pool_gated(k: np.ndarray, gate: np.ndarray, ape: np.ndarray, dtype: str, cu_seqlens: np.ndarray, kpool: int,
+               lib=None) -> np.ndarray:
+    """Gated pooled keys [P, d] (float32 values rounded to the input dtype): per pool and channel a
+    softmax over the pool's positions of gate [T, d] weights k + ape (ape [kpool, d])."""
+    k = _elem(k, dtype)
+    gate = np.ascontiguousarray(gate, dtype=np.float32)
+    ape = np.ascontiguousarray(ape, dtype=np.float32)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    d = k.shape[-1]
+    if gate.shape != (k.shape[0], d) or ape.shape != (kpool, d):
+        raise ValueError("gate must be [T, d] and ape [kpool, d]")
+    P = int(pool_offsets(cu, kpool, lib)[-1])
+    out = np.zeros((P, d), dtype=np.float32)
+    rc = _load(lib).kpool_oracle_pool_gated(_ptr(k), DTYPES[dtype], _ptr(gate), _ptr(ape), _ptr(cu), len(cu) - 1, d,
+                                            kpool, _ptr(out))
     if rc != 0:
         raise ValueError("invalid pooling arguments")
     return out

@@ -37,6 +37,12 @@ MUTANTS = {
     "bf16_truncate": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;", ""),
     "bf16_ties_away": ("(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
     "pool_reads_wrong_key": ("(start + p * kpool + j) * head_dim + c", "(start + p * kpool) * head_dim + c"),
+    "gated_unnormalised": ("exp((double)gate[(t0 + j) * head_dim + c] - m) / den;",
+                           "exp((double)gate[(t0 + j) * head_dim + c] - m);"),
+    "gated_ape_per_channel_only": ("(double)ape[(int64_t)j * head_dim + c]", "(double)ape[c]"),
+    "gated_ape_dropped": (" + (double)ape[(int64_t)j * head_dim + c])", ")"),
+    "gated_gate_of_first_token": ("double wj = exp((double)gate[(t0 + j) * head_dim + c] - m) / den;",
+                                  "double wj = exp((double)gate[t0 * head_dim + c] - m) / den;"),
     "budget_one_short": ("const int64_t kept = eligible < budget ? eligible : budget;",
                          "const int64_t kept = eligible < budget ? eligible : budget - 1;"),
 }
@@ -55,6 +61,10 @@ PIN_CALLS = [
     lambda lib: pins.test_invariants_ragged_packed(31, lib=lib),
     lambda lib: pins.test_short_rows_and_empty_sequences(lib=lib),
     lambda lib: pins.test_packed_equals_alone(lib=lib),
+    lambda lib: pins.test_gated_pool_hand_example("f32", lib=lib),
+    lambda lib: pins.test_gated_pool_hand_example("bf16", lib=lib),
+    lambda lib: pins.test_gated_pool_zero_gate_zero_ape_is_the_mean("bf16", lib=lib),
+    lambda lib: pins.test_gated_pool_one_hot_gate_picks_a_position(lib=lib),
 ]
 
 

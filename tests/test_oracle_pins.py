@@ -390,3 +390,71 @@ def test_tie_heavy_recipe_has_cutoff_ties():
             tied_in = ids[S[t, ids] == cut]
             assert unchosen[S[t, unchosen] == cut].min() > tied_in.max()
     assert straddling > 0
+
+
+# ---- gated pooling (a stated reading of the pages' compress gate / position embedding)
+#
+# kp[p,c] = sum_j softmax_j(gate[t_j,c]) * (k[t_j,c] + ape[j,c]); the pins below fix it
+# by hand-worked values, by its reduction to the mean, and by a one-hot gate that must
+# pick exactly one position per channel.
+
+def _bits_bf16(x: torch.Tensor) -> np.ndarray:
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gated_pool_hand_example(dtype, lib=None):
+    # one pool of two tokens, two channels: channel 0 weights (3/4, 1/4), channel 1 (1/4, 3/4)
+    k = torch.tensor([[4.0, 8.0], [8.0, 16.0]])
+    gate = np.array([[math.log(3.0), 0.0], [0.0, math.log(3.0)]], dtype=np.float32)
+    ape = np.array([[1.0, 0.0], [0.0, 2.0]], dtype=np.float32)
+    kk = _bits_bf16(k) if dtype == "bf16" else k.numpy()
+    out = oracle.pool_gated(kk, gate, ape, dtype, np.array([0, 2], dtype=np.int32), 2, lib=lib)
+    # 3/4 (4 + 1) + 1/4 (8 + 0) = 5.75 and 1/4 (8 + 0) + 3/4 (16 + 2) = 15.5
+    np.testing.assert_allclose(out, [[5.75, 15.5]], rtol=1e-6)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gated_pool_zero_gate_zero_ape_is_the_mean(dtype, lib=None):
+    g = torch.Generator().manual_seed(31)
+    cu = np.array([0, 37, 37, 100], dtype=np.int32)
+    k = torch.randint(-2, 3, (100, 8), generator=g).to(torch.float32)
+    kk = _bits_bf16(k) if dtype == "bf16" else k.numpy()
+    for kpool in (1, 3, 4):
+        gated = oracle.pool_gated(kk, np.zeros((100, 8), np.float32), np.zeros((kpool, 8), np.float32), dtype, cu,
+                                  kpool, lib=lib)
+        np.testing.assert_array_equal(gated, oracle.pool(kk, dtype, cu, kpool, lib=lib))
+
+
+def test_gated_pool_one_hot_gate_picks_a_position(lib=None):
+    """A gate that is 0 at one position and -1e4 elsewhere makes the softmax one-hot: the
+    pooled channel is that token's key plus that position's embedding (channel c picks
+    position c mod kpool, so a position/channel mix-up shows)."""
+    kpool, d, T = 4, 8, 24
+    g = torch.Generator().manual_seed(5)
+    k = torch.randn((T, d), generator=g)
+    ape = torch.randn((kpool, d), generator=g).numpy()
+    gate = np.full((T, d), -1e4, dtype=np.float32)
+    for t in range(T):
+        for c in range(d):
+            if t % kpool == c % kpool:
+                gate[t, c] = 0.0
+    out = oracle.pool_gated(k.numpy(), gate, ape, "f32", np.array([0, T], dtype=np.int32), kpool, lib=lib)
+    kn = k.numpy()
+    for p in range(T // kpool):
+        for c in range(d):
+            j = c % kpool
+            assert out[p, c] == np.float32(np.float64(kn[p * kpool + j, c]) + np.float64(ape[j, c]))
+
+
+def test_gated_pool_shift_invariance(lib=None):
+    """Adding a constant to a pool's gate scores (per channel) leaves the softmax unchanged."""
+    kpool, d, T = 4, 16, 64
+    g = torch.Generator().manual_seed(8)
+    k = _bits_bf16(torch.randn((T, d), generator=g))
+    gate = (torch.randn((T, d), generator=g) * 2).numpy()
+    ape = (torch.randn((kpool, d), generator=g) * 0.1).numpy()
+    cu = np.array([0, T], dtype=np.int32)
+    a = oracle.pool_gated(k, gate, ape, "bf16", cu, kpool, lib=lib)
+    b = oracle.pool_gated(k, gate + np.float32(3.0), ape, "bf16", cu, kpool, lib=lib)
+    np.testing.assert_array_equal(a, b)
