@@ -133,6 +133,41 @@ kpool_status kpool_pool_keys(const void* k, const int32_t* cu_seqlens, int32_t n
                              void* out_pooled_keys, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Step 1 with gated pooling instead of the mean. The pages name a per-token,
+ * per-channel compress gate (index_kpool_compress_gate, [head_dim, hidden]) and a
+ * per-position embedding (index_kpool_compress_ape, [kpool, head_dim]) in the
+ * GLM-5.3 DSA shard plan ("spark_model/layers/glm5next_dsa/tp.rs") and pass
+ * "gate scores" to the fused top-k ("NVIDIA/Megatron-LM pull request #8299",
+ * section "Mechanism"), but give no formula; this library reads them as gated
+ * compression:
+ *     kp[p,c] = sum_j softmax_j(gate[t_j,c]) * (k[t_j,c] + ape[j,c]),
+ * t_j the pool's j-th token, computed in fp32 and rounded to the key dtype. A
+ * zero gate and embedding reproduce the mean pooling bit for bit.
+ *   gate  [T, d] fp32 (the gate scores, already projected from the hidden state)
+ *   ape   [kpool, d] fp32
+ * Output and workspace as for kpool_pool_keys. Feed the result to
+ * kpool_select_pooled.
+ */
+kpool_status kpool_pool_keys_gated(const void* k, const float* gate, const float* ape, const int32_t* cu_seqlens,
+                                   int32_t num_seqs, int64_t total_tokens, int32_t head_dim, kpool_dtype dtype,
+                                   int32_t kpool, void* out_pooled_keys, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+/*
+ * kpool_select_ex for pooled keys the caller already has (from kpool_pool_keys,
+ * kpool_pool_keys_gated or a cache): steps 2-4 only. pooled_keys holds
+ * floor(T/kpool) * d elements of dtype (the size kpool_pool_keys writes into),
+ * the first P rows being the pools of cu_seqlens back to back; it is 16-byte
+ * aligned and non-NULL even when no sequence holds a complete pool. Same workspace and
+ * options as kpool_select_ex; the stage event after the pooling step is recorded
+ * right after the planning one.
+ */
+kpool_status kpool_select_pooled(const void* q, const void* pooled_keys, const float* w, const int32_t* cu_seqlens,
+                                 int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                                 kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                                 int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                                 void* workspace, size_t workspace_bytes, void* stream,
+                                 const kpool_options* options);
+/*
  * Step 4 alone: expands pool ids [T, budget] (as kpool_select writes them) into
  * token ids [T, index_topk + kpool], appending each row's tail and applying the
  * causal/varlen mask. Ids outside [0, floor((t+1)/kpool)) are treated as -1.

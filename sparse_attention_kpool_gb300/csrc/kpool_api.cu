@@ -88,12 +88,17 @@ size_t kpool_workspace_bytes(int64_t total_tokens, int32_t num_seqs, int32_t hea
   return workspace_layout(total_tokens, num_seqs, head_dim, elem_bytes(dtype), kpool).total;
 }
 
-kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
-                             int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
-                             kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
-                             int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
-                             void* workspace, size_t workspace_bytes, void* stream_ptr,
-                             const kpool_options* options) {
+}  // extern "C"
+
+namespace {
+
+// The whole selection; pools k itself when `pooled_in` is null, else scores the
+// caller's pooled keys (k unused).
+kpool_status select_impl(const void* q, const void* k, const void* pooled_in, const float* w,
+                         const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t heads,
+                         int32_t head_dim, kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                         int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores, void* workspace,
+                         size_t workspace_bytes, void* stream_ptr, const kpool_options* options) {
   kpool_options opt{};
   if (options) opt = *options;
   for (int i = 0; i < 4; ++i)
@@ -107,9 +112,10 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
   const int32_t budget = index_topk / kpool;
   const int64_t T = total_tokens;
   if (T == 0) return KPOOL_OK;
-  if (!q || !k || !w || !cu_seqlens || !out_token_ids || (budget > 0 && !out_pool_ids))
+  const void* kin = pooled_in ? pooled_in : k;
+  if (!q || !kin || !w || !cu_seqlens || !out_token_ids || (budget > 0 && !out_pool_ids))
     return KPOOL_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(w, 4) || !aligned(cu_seqlens, 4) ||
+  if (!aligned(q, 16) || !aligned(kin, 16) || !aligned(w, 4) || !aligned(cu_seqlens, 4) ||
       !aligned(out_pool_ids, 4) || !aligned(out_token_ids, 4) || !aligned(out_pool_scores, 4))
     return KPOOL_ERR_INVALID_ARG;
 
@@ -138,7 +144,7 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
   int sms = 0;
   if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  void* pooled = ws + L.pooled;
+  const void* pooled = pooled_in ? pooled_in : static_cast<const void*>(ws + L.pooled);
 
   void* const* ev = opt.stage_events;
   auto mark = [&](int i) {
@@ -146,9 +152,10 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
   };
   if (!mark(0)) return KPOOL_ERR_CUDA;
   if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, T, kpool, ws, L, stream)) || !mark(1)) return KPOOL_ERR_CUDA;
-  if (!cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, pooled, ws, L, sms, stream)) ||
-      !mark(2))
+  if (!pooled_in &&
+      !cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, ws + L.pooled, ws, L, sms, stream)))
     return KPOOL_ERR_CUDA;
+  if (!mark(2)) return KPOOL_ERR_CUDA;
   if (budget > 0) {
     cudaError_t e;
     if (use_tc) {
@@ -168,6 +175,32 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
       !mark(4))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
+                             int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                             kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                             int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                             void* workspace, size_t workspace_bytes, void* stream_ptr,
+                             const kpool_options* options) {
+  return select_impl(q, k, nullptr, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool,
+                     index_topk, scale, out_pool_ids, out_token_ids, out_pool_scores, workspace, workspace_bytes,
+                     stream_ptr, options);
+}
+
+kpool_status kpool_select_pooled(const void* q, const void* pooled_keys, const float* w, const int32_t* cu_seqlens,
+                                 int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                                 kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                                 int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
+                                 void* workspace, size_t workspace_bytes, void* stream_ptr,
+                                 const kpool_options* options) {
+  return select_impl(q, nullptr, pooled_keys, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool,
+                     index_topk, scale, out_pool_ids, out_token_ids, out_pool_scores, workspace, workspace_bytes,
+                     stream_ptr, options);
 }
 
 kpool_status kpool_select(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
@@ -198,6 +231,32 @@ kpool_status kpool_pool_keys(const void* k, const int32_t* cu_seqlens, int32_t n
   if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, ws, L, stream))) return KPOOL_ERR_CUDA;
   if (!cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool, out_pooled_keys, ws, L,
                            sms, stream)))
+    return KPOOL_ERR_CUDA;
+  return KPOOL_OK;
+}
+
+kpool_status kpool_pool_keys_gated(const void* k, const float* gate, const float* ape, const int32_t* cu_seqlens,
+                                   int32_t num_seqs, int64_t total_tokens, int32_t head_dim, kpool_dtype dtype,
+                                   int32_t kpool, void* out_pooled_keys, void* workspace, size_t workspace_bytes,
+                                   void* stream_ptr) {
+  kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
+  if (st != KPOOL_OK) return st;
+  if (total_tokens == 0) return KPOOL_OK;
+  if (!k || !gate || !ape || !cu_seqlens || (total_tokens / kpool > 0 && !out_pooled_keys))
+    return KPOOL_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(out_pooled_keys, 16) || !aligned(gate, 4) || !aligned(ape, 4) ||
+      !aligned(cu_seqlens, 4))
+    return KPOOL_ERR_INVALID_ARG;
+  const WorkspaceLayout L = workspace_layout(total_tokens, num_seqs, head_dim, elem_bytes(dtype), kpool);
+  st = check_workspace(workspace, workspace_bytes, L);
+  if (st != KPOOL_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int sms = 0;
+  if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, ws, L, stream))) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_pool_gated(k, gate, ape, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool,
+                                 out_pooled_keys, ws, L, sms, stream)))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
 }

@@ -104,6 +104,11 @@ cudaError_t launch_pool(const void* k, kpool_dtype dtype, const int32_t* cu, int
                         int32_t d, int32_t kpool, void* out, const char* ws, const WorkspaceLayout& L,
                         int num_sms, cudaStream_t stream);
 
+// K1, gated: kp[p,c] = sum_j softmax_j(gate[t_j,c]) * (k[t_j,c] + ape[j,c]).
+cudaError_t launch_pool_gated(const void* k, const float* gate, const float* ape, kpool_dtype dtype,
+                              const int32_t* cu, int32_t S, int64_t T, int32_t d, int32_t kpool, void* out,
+                              const char* ws, const WorkspaceLayout& L, int num_sms, cudaStream_t stream);
+
 // K2 (CUDA cores): any supported shape.
 cudaError_t launch_select_simt(const void* q, const void* kp, const float* w, kpool_dtype dtype,
                                const int32_t* cu, int32_t S, int64_t T, int32_t H, int32_t d, int32_t kpool,

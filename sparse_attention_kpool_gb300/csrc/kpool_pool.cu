@@ -90,7 +90,85 @@ __global__ void __launch_bounds__(256) pool_kernel(const T* __restrict__ k, cons
   }
 }
 
+// Gated pooling, the library's reading of the pages' compress gate and position
+// embedding (parameters index_kpool_compress_gate [head_dim, hidden] and
+// index_kpool_compress_ape [kpool, head_dim] in the GLM-5.3 DSA shard plan,
+// "spark_model/layers/glm5next_dsa/tp.rs"; "gate scores" passed to the fused
+// top-k in "NVIDIA/Megatron-LM pull request #8299", section "Mechanism"):
+//   kp[p,c] = sum_j softmax_j(gate[t_j,c]) * (k[t_j,c] + ape[j,c]),  t_j = first + j,
+// in fp32 (max-subtracted exponentials, the normalisation applied once at the end),
+// rounded to the key dtype. A zero gate and embedding give exactly the mean pooling.
+template <typename T>
+__global__ void __launch_bounds__(256) pool_gated_kernel(const T* __restrict__ k, const float* __restrict__ gate,
+                                                         const float* __restrict__ ape,
+                                                         const int32_t* __restrict__ cu,
+                                                         const int32_t* __restrict__ pool_off,
+                                                         const WorkspaceHeader* __restrict__ hdr, int S, int d,
+                                                         int kpool, T* __restrict__ out) {
+  constexpr int V = Vec<T>::kLanes;
+  if (hdr->error != 0) return;
+  const int64_t P = hdr->total_pools;
+  const int chunks = d / V;
+  const int64_t total = P * chunks;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t g = i / chunks;  // global pool row
+    const int c = int(i - g * chunks) * V;
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (int64_t(__ldg(pool_off + mid)) <= g) lo = mid; else hi = mid - 1;
+    }
+    const int64_t first = int64_t(__ldg(cu + lo)) + (g - __ldg(pool_off + lo)) * kpool;
+    float m[8], den[8], num[8];
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      m[e] = -INFINITY;
+      den[e] = 0.0f;
+      num[e] = 0.0f;
+    }
+    for (int j = 0; j < kpool; ++j)
+#pragma unroll
+      for (int e = 0; e < V; ++e) m[e] = fmaxf(m[e], __ldg(gate + (first + j) * d + c + e));
+    for (int j = 0; j < kpool; ++j) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(k + (first + j) * d + c));
+      float f[8];
+      unpack(v, f, static_cast<T*>(nullptr));
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const float ge = expf(__ldg(gate + (first + j) * d + c + e) - m[e]);
+        den[e] = __fadd_rn(den[e], ge);
+        num[e] = __fadd_rn(num[e], __fmul_rn(ge, __fadd_rn(f[e], __ldg(ape + int64_t(j) * d + c + e))));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) num[e] = __fdiv_rn(num[e], den[e]);
+    *reinterpret_cast<uint4*>(out + g * d + c) = pack(num, static_cast<T*>(nullptr));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_pool_gated(const void* k, const float* gate, const float* ape, kpool_dtype dtype,
+                              const int32_t* cu, int32_t S, int64_t T, int32_t d, int32_t kpool, void* out,
+                              const char* ws, const WorkspaceLayout& L, int num_sms, cudaStream_t stream) {
+  const int64_t max_chunks = (T / kpool) * (d / (dtype == KPOOL_BF16 ? 8 : 4));
+  if (max_chunks == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (max_chunks + threads - 1) / threads;
+  const int64_t cap = int64_t(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  const auto* hdr = reinterpret_cast<const WorkspaceHeader*>(ws + L.header);
+  const auto* pool_off = reinterpret_cast<const int32_t*>(ws + L.pool_off);
+  if (dtype == KPOOL_BF16)
+    pool_gated_kernel<__nv_bfloat16><<<unsigned(blocks), threads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(k), gate, ape, cu, pool_off, hdr, S, d, kpool,
+        static_cast<__nv_bfloat16*>(out));
+  else
+    pool_gated_kernel<float><<<unsigned(blocks), threads, 0, stream>>>(static_cast<const float*>(k), gate, ape, cu,
+                                                                       pool_off, hdr, S, d, kpool,
+                                                                       static_cast<float*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pool(const void* k, kpool_dtype dtype, const int32_t* cu, int32_t S, int64_t T, int32_t d,
                         int32_t kpool, void* out, const char* ws, const WorkspaceLayout& L, int num_sms,

@@ -39,6 +39,7 @@ EXPORTED = (
     "kpool_workspace_bytes", "kpool_select", "kpool_select_ex", "kpool_pool_keys", "kpool_expand",
     "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string", "kpool_last_cuda_error",
     "kpool_select_static_scratch", "kpool_rows_workspace_bytes", "kpool_select_rows", "kpool_select_rows_ex",
+    "kpool_pool_keys_gated", "kpool_select_pooled",
 )
 KPOOL_STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -102,6 +103,10 @@ def load() -> ctypes.CDLL:
         lib.kpool_select_rows.restype = i32
         lib.kpool_select_rows_ex.argtypes = lib.kpool_select_rows.argtypes + [ctypes.POINTER(kpool_options)]
         lib.kpool_select_rows_ex.restype = i32
+        lib.kpool_pool_keys_gated.argtypes = [P, P, P, P, i32, i64, i32, i32, i32, P, P, sz, P]
+        lib.kpool_pool_keys_gated.restype = i32
+        lib.kpool_select_pooled.argtypes = sel + [ctypes.POINTER(kpool_options)]
+        lib.kpool_select_pooled.restype = i32
         _lib = lib
         return lib
 
@@ -323,4 +328,57 @@ def kpool_select_rows(q: torch.Tensor, w: torch.Tensor, row_seq: torch.Tensor, r
                                      _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts))
     if st != KPOOL_OK:
         raise KpoolError(st, "kpool_select_rows")
+    return out_pool_ids, out_token_ids, out_pool_scores
+
+
+def kpool_pool_keys_gated(k: torch.Tensor, gate: torch.Tensor, ape: torch.Tensor, cu_seqlens: torch.Tensor,
+                          kpool: int, out=None, workspace=None, stream=None):
+    """Gated pooled keys (see kpool_pool_keys_gated in kpool.h): k [T,d], gate [T,d] fp32,
+    ape [kpool,d] fp32 -> [T // kpool, d] whose first P rows are the pools."""
+    T, d = k.shape
+    S = cu_seqlens.numel() - 1
+    dt = _dtype_code(k)
+    if gate.dtype != torch.float32 or ape.dtype != torch.float32 or tuple(gate.shape) != (T, d) \
+            or tuple(ape.shape) != (kpool, d):
+        raise TypeError("gate must be float32 [T, d] and ape float32 [kpool, d]")
+    if out is None:
+        out = torch.empty((max(T // kpool, 0), d), dtype=k.dtype, device=k.device)
+    if workspace is None:
+        workspace = new_workspace(T, S, 1, d, dt, kpool, 0, k.device)
+    _check_cuda(k, gate, ape, cu_seqlens, out, workspace)
+    st = load().kpool_pool_keys_gated(_ptr(k), _ptr(gate), _ptr(ape), _ptr(cu_seqlens), S, T, d, dt, kpool, _ptr(out),
+                                      _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_pool_keys_gated")
+    return out
+
+
+def kpool_select_pooled(q: torch.Tensor, pooled_keys: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor,
+                        kpool: int, index_topk: int, scale: float, out_pool_ids=None, out_token_ids=None,
+                        out_pool_scores=None, return_scores: bool = False, workspace=None, stream=None,
+                        score_kernel: int = KPOOL_SCORE_AUTO, max_ctas: int = 0):
+    """Selection from pooled keys the caller already has (steps 2-4); q [T,H,d], pooled_keys [>= P, d]."""
+    T, H, d = q.shape
+    S = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    if pooled_keys.dtype != q.dtype or w.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("pooled_keys must match q's dtype; w must be float32; cu_seqlens int32")
+    B = index_topk // kpool if kpool > 0 else 0
+    dev = q.device
+    if out_pool_ids is None:
+        out_pool_ids = torch.empty((T, B), dtype=torch.int32, device=dev)
+    if out_token_ids is None:
+        out_token_ids = torch.empty((T, index_topk + kpool), dtype=torch.int32, device=dev)
+    if out_pool_scores is None and return_scores:
+        out_pool_scores = torch.empty((T, B), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(T, S, H, d, dt, kpool, index_topk, dev)
+    _check_cuda(q, pooled_keys, w, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores, workspace)
+    opts = kpool_options(score_kernel, max_ctas)
+    st = load().kpool_select_pooled(_ptr(q), _ptr(pooled_keys), _ptr(w), _ptr(cu_seqlens), S, T, H, d, dt, kpool,
+                                    index_topk, float(scale), _ptr(out_pool_ids), _ptr(out_token_ids),
+                                    _ptr(out_pool_scores), _ptr(workspace), workspace.numel(), _stream(stream),
+                                    ctypes.byref(opts))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_select_pooled")
     return out_pool_ids, out_token_ids, out_pool_scores

@@ -178,6 +178,30 @@ def test_select_rows_rejects_bad_arguments(lib):
     assert _rows(lib, R=0, q=0, w=0, rs=0, rp=0, kp=0, ids=0, toks=0, ws=0) == K.KPOOL_OK
 
 
+def test_gated_pool_and_pooled_select_validation(lib):
+    P = ctypes.c_void_p
+    ok = dict(k=P(FAKE), g=P(FAKE), a=P(FAKE), cu=P(FAKE), out=P(FAKE), ws=P(FAKE))
+
+    def gated(**kw):
+        v = dict(ok, **kw)
+        return lib.kpool_pool_keys_gated(v["k"], v["g"], v["a"], v["cu"], 1, 64, 32, K.KPOOL_F32, 4, v["out"],
+                                         v["ws"], 1 << 20, None)
+    assert gated(g=None) == K.KPOOL_ERR_INVALID_ARG
+    assert gated(a=None) == K.KPOOL_ERR_INVALID_ARG
+    assert gated(g=P(FAKE + 2)) == K.KPOOL_ERR_INVALID_ARG
+    assert gated(k=P(FAKE + 4)) == K.KPOOL_ERR_INVALID_ARG
+    assert gated(ws=None) == K.KPOOL_ERR_WORKSPACE
+    assert lib.kpool_pool_keys_gated(None, None, None, None, 0, 0, 32, K.KPOOL_F32, 4, None, None, 0,
+                                     None) == K.KPOOL_OK
+    # the pooled select validates like kpool_select_ex, with the pooled keys in k's place
+    assert lib.kpool_select_pooled(P(FAKE), None, P(FAKE), P(FAKE), 1, 64, 4, 32, K.KPOOL_F32, 4, 16, 0.5,
+                                   P(FAKE), P(FAKE), None, P(FAKE), 1 << 20, None, None) == K.KPOOL_ERR_INVALID_ARG
+    assert lib.kpool_select_pooled(P(FAKE), P(FAKE + 8), P(FAKE), P(FAKE), 1, 64, 4, 32, K.KPOOL_F32, 4, 16, 0.5,
+                                   P(FAKE), P(FAKE), None, P(FAKE), 1 << 20, None, None) == K.KPOOL_ERR_INVALID_ARG
+    assert lib.kpool_select_pooled(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, 64, 4, 32, K.KPOOL_F32, 4, 16, 0.5,
+                                   P(FAKE), P(FAKE), None, None, 1 << 20, None, None) == K.KPOOL_ERR_WORKSPACE
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(K, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(K, "_lib", None)
