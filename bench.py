@@ -510,6 +510,26 @@ def main():
     value = world * pairs / (ms_step / 1e3)
     k_ms = [statistics.median(x) for x in per_kernel]  # per-kernel medians over the timed steps
 
+    # ---- the gated pooling variant of step 1 (kpool_pool_keys_gated), timed on its own
+    gg = torch.Generator(device=dev)
+    gg.manual_seed(wl.seed + 101)
+    gate = torch.randn((T, d), generator=gg, device=dev) * 2.0
+    ape = torch.randn((wl.kpool, d), generator=gg, device=dev) * 0.25
+    kp_g = torch.empty((T // wl.kpool, d), dtype=inp["k"].dtype, device=dev)
+    gws = K.new_workspace(T, wl.num_seqs, 1, d, K.KPOOL_BF16 if wl.dtype == "bf16" else K.KPOOL_F32, wl.kpool, 0, dev)
+    for _ in range(args.warmup):
+        K.kpool_pool_keys_gated(inp["k"], gate, ape, inp["cu_seqlens"], wl.kpool, out=kp_g, workspace=gws,
+                                stream=stream)
+    ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ga.record(stream)
+    for _ in range(args.steps):
+        K.kpool_pool_keys_gated(inp["k"], gate, ape, inp["cu_seqlens"], wl.kpool, out=kp_g, workspace=gws,
+                                stream=stream)
+    gb.record(stream)
+    torch.cuda.synchronize()
+    gated_ms = ga.elapsed_time(gb) / args.steps  # plan + gated pooling
+    del gate, kp_g, gws
+
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
@@ -561,6 +581,7 @@ def main():
     kp_bytes = wl.num_pools() * d * 2
     k1_bytes = T * d * 2 + kp_bytes
     k3_bytes = T * B * 4 + T * Wd * 4
+    kg_bytes = T * d * 2 + T * d * 4 + wl.kpool * d * 4 + kp_bytes  # keys, fp32 gate scores, embedding in; pools out
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -582,7 +603,10 @@ def main():
             "pool": {"bytes": k1_bytes, "GB/s": k1_bytes / (k_ms[1] / 1e3) / 1e9,
                      "frac": k1_bytes / (k_ms[1] / 1e3) / 1e9 / hbm},
             "expand": {"bytes": k3_bytes, "GB/s": k3_bytes / (k_ms[3] / 1e3) / 1e9,
-                       "frac": k3_bytes / (k_ms[3] / 1e3) / 1e9 / hbm}},
+                       "frac": k3_bytes / (k_ms[3] / 1e3) / 1e9 / hbm},
+            "pool_gated": {"bytes": kg_bytes, "ms": gated_ms, "GB/s": kg_bytes / (gated_ms / 1e3) / 1e9,
+                           "frac": kg_bytes / (gated_ms / 1e3) / 1e9 / hbm,
+                           "note": "kpool_pool_keys_gated (plan + gated pooling), not part of the timed step"}},
         "clocks": clock_info,
         "gpu_launches": 4 * args.steps,
         "e2e": e2e,
