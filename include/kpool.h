@@ -143,8 +143,9 @@ kpool_status kpool_pool_keys(const void* k, const int32_t* cu_seqlens, int32_t n
  *     kp[p,c] = sum_j softmax_j(gate[t_j,c]) * (k[t_j,c] + ape[j,c]),
  * t_j the pool's j-th token, computed in fp32 and rounded to the key dtype. A
  * zero gate and embedding reproduce the mean pooling bit for bit.
- *   gate  [T, d] fp32 (the gate scores, already projected from the hidden state)
- *   ape   [kpool, d] fp32
+ *   gate  [T, d] fp32, 16-byte aligned (the gate scores, already projected from
+ *         the hidden state)
+ *   ape   [kpool, d] fp32, 16-byte aligned
  * Output and workspace as for kpool_pool_keys. Feed the result to
  * kpool_select_pooled.
  */

@@ -244,7 +244,7 @@ kpool_status kpool_pool_keys_gated(const void* k, const float* gate, const float
   if (total_tokens == 0) return KPOOL_OK;
   if (!k || !gate || !ape || !cu_seqlens || (total_tokens / kpool > 0 && !out_pooled_keys))
     return KPOOL_ERR_INVALID_ARG;
-  if (!aligned(k, 16) || !aligned(out_pooled_keys, 16) || !aligned(gate, 4) || !aligned(ape, 4) ||
+  if (!aligned(k, 16) || !aligned(out_pooled_keys, 16) || !aligned(gate, 16) || !aligned(ape, 16) ||
       !aligned(cu_seqlens, 4))
     return KPOOL_ERR_INVALID_ARG;
   const WorkspaceLayout L = workspace_layout(total_tokens, num_seqs, head_dim, elem_bytes(dtype), kpool);

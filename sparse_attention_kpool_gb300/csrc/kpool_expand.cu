@@ -45,6 +45,33 @@ __device__ __forceinline__ int32_t token_at(const RowInfo& ri, int32_t pool, int
   return int32_t(tok);
 }
 
+// kpool == 4 (16 bytes of tokens per pool): one warp per row, lane l writes the
+// row's 16-byte chunks l, l + 32, ...; chunk j < budget expands pool rank j, chunk
+// budget holds the tail. 32-bit arithmetic throughout.
+__global__ void __launch_bounds__(256) expand_kernel_k4(const int32_t* __restrict__ pool_ids,
+                                                        const int32_t* __restrict__ cu, int S, int64_t T,
+                                                        int budget, int32_t* __restrict__ out,
+                                                        const WorkspaceHeader* __restrict__ hdr) {
+  if (hdr != nullptr && hdr->error != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  const int64_t W4 = int64_t(budget) + 1;  // 16-byte chunks per row
+  for (int64_t row = int64_t(blockIdx.x) * warps + (threadIdx.x >> 5); row < T; row += int64_t(gridDim.x) * warps) {
+    const int b = seq_of_row(cu, S, row);
+    const int t = int(row - __ldg(cu + b));
+    const int e = (t + 1) >> 2, tail = (t + 1) & 3;
+    const int32_t* ids = pool_ids + row * budget;
+    int4* dst = reinterpret_cast<int4*>(out + row * (W4 * 4));
+    for (int j = lane; j < budget; j += 32) {
+      const int32_t id = __ldg(ids + j);
+      dst[j] = (id >= 0 && id < e) ? make_int4(4 * id, 4 * id + 1, 4 * id + 2, 4 * id + 3)
+                                   : make_int4(-1, -1, -1, -1);
+    }
+    if (lane == 0)
+      dst[budget] = make_int4(tail > 0 ? 4 * e : -1, tail > 1 ? 4 * e + 1 : -1, tail > 2 ? 4 * e + 2 : -1, -1);
+  }
+}
+
 __global__ void __launch_bounds__(256) expand_kernel_vec4(const int32_t* __restrict__ pool_ids,
                                                           const int32_t* __restrict__ cu, int S, int64_t T,
                                                           int kpool, int budget, int32_t* __restrict__ out,
@@ -97,7 +124,11 @@ cudaError_t launch_expand(const int32_t* pool_ids, const int32_t* cu, int32_t S,
   const int64_t cap = int64_t(num_sms) * 16;
   if (blocks > cap) blocks = cap;
   const bool vec = (kpool % 4 == 0) && (reinterpret_cast<uintptr_t>(out_tokens) % 16 == 0);
-  if (vec)
+  if (vec && kpool == 4) {
+    int64_t b4 = (T + 7) / 8;  // 8 rows (warps) per CTA
+    if (b4 > int64_t(num_sms) * 16) b4 = int64_t(num_sms) * 16;
+    expand_kernel_k4<<<unsigned(b4), 256, 0, stream>>>(pool_ids, cu, S, T, budget, out_tokens, hdr);
+  } else if (vec)
     expand_kernel_vec4<<<unsigned(blocks), 256, 0, stream>>>(pool_ids, cu, S, T, kpool, budget, out_tokens, hdr);
   else
     expand_kernel_scalar<<<unsigned(blocks), 256, 0, stream>>>(pool_ids, cu, S, T, kpool, budget, out_tokens,

@@ -126,18 +126,66 @@ __global__ void __launch_bounds__(256) pool_gated_kernel(const T* __restrict__ k
       den[e] = 0.0f;
       num[e] = 0.0f;
     }
-    for (int j = 0; j < kpool; ++j)
+    // gate scores of the chunk's V channels, 16-byte loads; kept for the second pass
+    // when the pool is short enough to hold in registers
+    constexpr int kHold = 4;
+    float gh[kHold][8];
+    for (int j = 0; j < kpool; ++j) {
+      float gv[8];
+      const float4* gp = reinterpret_cast<const float4*>(gate + (first + j) * d + c);
 #pragma unroll
-      for (int e = 0; e < V; ++e) m[e] = fmaxf(m[e], __ldg(gate + (first + j) * d + c + e));
+      for (int h = 0; h < V / 4; ++h) {
+        const float4 x = __ldg(gp + h);
+        gv[4 * h] = x.x;
+        gv[4 * h + 1] = x.y;
+        gv[4 * h + 2] = x.z;
+        gv[4 * h + 3] = x.w;
+      }
+#pragma unroll
+      for (int e = 0; e < V; ++e) m[e] = fmaxf(m[e], gv[e]);
+#pragma unroll
+      for (int hj = 0; hj < kHold; ++hj)
+        if (hj == j)
+#pragma unroll
+          for (int e = 0; e < V; ++e) gh[hj][e] = gv[e];
+    }
     for (int j = 0; j < kpool; ++j) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(k + (first + j) * d + c));
       float f[8];
       unpack(v, f, static_cast<T*>(nullptr));
+      float gv[8];
+      if (j < kHold) {
+#pragma unroll
+        for (int hj = 0; hj < kHold; ++hj)
+          if (hj == j)
+#pragma unroll
+            for (int e = 0; e < V; ++e) gv[e] = gh[hj][e];
+      } else {
+        const float4* gp = reinterpret_cast<const float4*>(gate + (first + j) * d + c);
+#pragma unroll
+        for (int h = 0; h < V / 4; ++h) {
+          const float4 x = __ldg(gp + h);
+          gv[4 * h] = x.x;
+          gv[4 * h + 1] = x.y;
+          gv[4 * h + 2] = x.z;
+          gv[4 * h + 3] = x.w;
+        }
+      }
+      const float4* ap = reinterpret_cast<const float4*>(ape + int64_t(j) * d + c);
+      float av[8];
+#pragma unroll
+      for (int h = 0; h < V / 4; ++h) {
+        const float4 x = __ldg(ap + h);
+        av[4 * h] = x.x;
+        av[4 * h + 1] = x.y;
+        av[4 * h + 2] = x.z;
+        av[4 * h + 3] = x.w;
+      }
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        const float ge = expf(__ldg(gate + (first + j) * d + c + e) - m[e]);
+        const float ge = expf(gv[e] - m[e]);
         den[e] = __fadd_rn(den[e], ge);
-        num[e] = __fadd_rn(num[e], __fmul_rn(ge, __fadd_rn(f[e], __ldg(ape + int64_t(j) * d + c + e))));
+        num[e] = __fadd_rn(num[e], __fmul_rn(ge, __fadd_rn(f[e], av[e])));
       }
     }
 #pragma unroll

@@ -189,6 +189,7 @@ def test_gated_pool_and_pooled_select_validation(lib):
     assert gated(g=None) == K.KPOOL_ERR_INVALID_ARG
     assert gated(a=None) == K.KPOOL_ERR_INVALID_ARG
     assert gated(g=P(FAKE + 2)) == K.KPOOL_ERR_INVALID_ARG
+    assert gated(a=P(FAKE + 8)) == K.KPOOL_ERR_INVALID_ARG  # 16-byte vector loads
     assert gated(k=P(FAKE + 4)) == K.KPOOL_ERR_INVALID_ARG
     assert gated(ws=None) == K.KPOOL_ERR_WORKSPACE
     assert lib.kpool_pool_keys_gated(None, None, None, None, 0, 0, 32, K.KPOOL_F32, 4, None, None, 0,
