@@ -22,7 +22,8 @@ struct WorkspaceHeader {
   int32_t n_items;      // work items written by the planning kernel
   int32_t n_levels;     // distinct item depths
   int32_t total_pools;  // P
-  int32_t reserved[60];
+  int32_t reserved[59];
+  int32_t next_item;    // work counter of the tensor-core kernel (reset by the planning kernel)
 };
 static_assert(sizeof(WorkspaceHeader) == 256, "header is one 256-byte block");
 

@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
       hdr->n_items = 0;
       hdr->n_levels = 0;
       hdr->total_pools = 0;
+      hdr->next_item = 0;
     }
     return;
   }
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
       hdr->n_items = 0;
       hdr->n_levels = 0;
       hdr->total_pools = 0;
+      hdr->next_item = 0;
     }
     return;
   }
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     hdr->n_items = n_items;
     hdr->n_levels = n_levels;
     hdr->total_pools = carry_p;
+    hdr->next_item = 0;
   }
 }
 

@@ -103,12 +103,14 @@ constexpr uint32_t kOffPool = kOffQ + kQBytes;
 constexpr uint32_t kOffCand = kOffPool + kStages * kStageBytes;
 constexpr uint32_t kOffW = kOffCand + kRows * kCap * 8;
 constexpr uint32_t kOffBar = kOffW + kRows * kHeads * 4;
-constexpr int kNumBars = 2 + 2 * kStages + 4 + 1;
+constexpr int kRing = 4;  // work items handed from the producer to the MMA issuer and the epilogue
+constexpr int kNumBars = 2 + 2 * kStages + 4 + 1 + 2 * kRing;
 constexpr uint32_t kOffCount = kOffBar + kNumBars * 8;         // [kRows][4] region counts
 constexpr uint32_t kOffTau = (kOffCount + kRows * 4 * 4 + 7) & ~7u;
 constexpr uint32_t kOffElig = kOffTau + kRows * 8;
 constexpr uint32_t kOffMisc = kOffElig + kRows * 4;
-constexpr uint32_t kOffSelect = kOffMisc + 16;              // SelectScratch
+constexpr uint32_t kOffRing = kOffMisc + 16;                // [kRing] item indices
+constexpr uint32_t kOffSelect = kOffRing + 4 * kRing;       // SelectScratch
 constexpr uint32_t kSelectBytes = (sizeof(SelectScratch) + 15) & ~size_t(15);
 constexpr uint32_t kSmemUsed = kOffSelect + 2 * kSelectBytes;  // one SelectScratch per epilogue group
 constexpr uint32_t kSmemBytes = kSmemUsed;
@@ -129,6 +131,8 @@ struct Bars {
   uint64_t* acc_full;   // [2]
   uint64_t* acc_empty;  // [2]
   uint64_t* mma_done;
+  uint64_t* ring_full;   // [kRing]: the producer wrote the slot's item index
+  uint64_t* ring_empty;  // [kRing]: the MMA issuer and the 8 epilogue warps read it
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t* base) {
@@ -141,6 +145,8 @@ __device__ __forceinline__ Bars bars_at(uint8_t* base) {
   r.acc_full = b + 2 + 2 * kStages;
   r.acc_empty = b + 4 + 2 * kStages;
   r.mma_done = b + 6 + 2 * kStages;
+  r.ring_full = b + 7 + 2 * kStages;
+  r.ring_empty = b + 7 + 2 * kStages + kRing;
   return r;
 }
 
@@ -173,10 +179,6 @@ struct Item {
   int32_t pool_base;  // global pooled-key row of the sequence's pool 0
   int32_t n_tiles;    // pool tiles covering the last row's eligible pools
 };
-
-__device__ __forceinline__ int item_index(int r, int cta, int grid) {
-  return r * grid + ((r & 1) ? (grid - 1 - cta) : cta);
-}
 
 __device__ __forceinline__ Item load_item(const int2* items, const int32_t* cu, const int32_t* pool_off, int idx,
                                           int kpool) {
@@ -212,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   int32_t* s_abort = reinterpret_cast<int32_t*>(smem + kOffMisc + 4);
   float* s_w = reinterpret_cast<float*>(smem + kOffW);
-  SelectScratch* s_sel = reinterpret_cast<SelectScratch*>(smem + kOffSelect);
   uint64_t* s_cand = reinterpret_cast<uint64_t*>(smem + kOffCand);
 
   // The 128-byte-swizzled TMA tiles need a 1024-byte aligned base. Every thread
@@ -238,6 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar.acc_empty + a, 8);
     }
     ptx::mbar_init(bar.mma_done, 1);
+    for (int i = 0; i < kRing; ++i) {
+      ptx::mbar_init(bar.ring_full + i, 1);
+      ptx::mbar_init(bar.ring_empty + i, 9);
+    }
     ptx::fence_mbar_init();
     *s_abort = 0;
     ptx::prefetch_tmap(&tmap_q);
@@ -252,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   volatile int32_t* abort_flag = s_abort;
+  volatile int32_t* s_ring = reinterpret_cast<volatile int32_t*>(smem + kOffRing);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -264,8 +270,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_armed = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int idx = item_index(r, blockIdx.x, gridDim.x);
-        if (idx >= n_items) break;
+        // next work item from the global counter (heaviest first, as the plan sorted
+        // them), handed to the MMA issuer and the epilogue through the ring
+        const int slot = r % kRing;
+        const uint32_t use = uint32_t(r / kRing);
+        if (use > 0 && !ptx::mbar_wait_bounded(bar.ring_empty + slot, (use - 1) & 1, kMaxPolls, kMaxWaitNs,
+                                               kBackoffNs)) {
+          ok = false;
+          break;
+        }
+        int idx = atomicAdd(&hdr->next_item, 1);
+        if (idx >= n_items) idx = -1;
+        s_ring[slot] = idx;
+        ptx::mbar_arrive(bar.ring_full + slot);
+        if (idx < 0) break;
         const Item it = load_item(items, cu, pool_off, idx, kpool);
         if (it.n_tiles == 0) continue;
         if (!ptx::mbar_wait_bounded(bar.q_empty, q_phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
@@ -318,8 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0, q_phase = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int idx = item_index(r, blockIdx.x, gridDim.x);
-        if (idx >= n_items) break;
+        const int slot = r % kRing;
+        if (!ptx::mbar_wait_bounded(bar.ring_full + slot, uint32_t(r / kRing) & 1, kMaxPolls, kMaxWaitNs,
+                                    kBackoffNs)) {
+          ok = false;
+          break;
+        }
+        const int idx = s_ring[slot];
+        ptx::mbar_arrive(bar.ring_empty + slot);
+        if (idx < 0) break;
         const Item it = load_item(items, cu, pool_off, idx, kpool);
         if (it.n_tiles == 0) continue;
         if (!ptx::mbar_wait_bounded(bar.q_full, q_phase, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
@@ -384,8 +409,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int r = 0;; ++r) {
-      const int idx = item_index(r, blockIdx.x, gridDim.x);
-      if (idx >= n_items) break;
+      // the next work item, as the producer fetched it
+      const int slot = r % kRing;
+      int idx = -1;
+      bool got = true;
+      if (lane == 0) {
+        got = ptx::mbar_wait_bounded(bar.ring_full + slot, uint32_t(r / kRing) & 1, kMaxPolls, kMaxWaitNs);
+        if (got) idx = s_ring[slot];
+        ptx::mbar_arrive(bar.ring_empty + slot);
+      }
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      // the group leaves together if any of its warps' waits ran out
+      if (named_bar_or(bar_id, 128, __shfl_sync(0xffffffffu, got ? 0 : 1, 0) != 0)) {
+        if (gt == 0) {
+          record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      if (idx < 0) break;
       const Item it = load_item(items, cu, pool_off, idx, kpool);
       // per-item state of the group's 4 rows
       {
