@@ -330,3 +330,19 @@ def test_bounded_wait_reports_timeout_without_hanging():
     inp = W.generate(wl, "cpu")
     ids, toks, _ = run(to_dev(inp), wl)
     parity.assert_exact(full_oracle(inp, wl), ids, toks)
+
+
+def test_many_empty_items_through_the_work_ring():
+    """Hundreds of sequences shorter than a pool (items with nothing to score) between a few
+    long ones: the producer hands every item through the four-slot ring, including long runs
+    of empty ones, on one CTA, on three and on the full grid. Bit-exact on integer data."""
+    g = torch.Generator().manual_seed(61)
+    lens = [int(x) for x in torch.randint(0, 4, (300,), generator=g)]
+    lens[17], lens[150], lens[299] = 1500, 700, 2100
+    wl = W.custom("ring", tuple(lens), 32, 128, 4, 256, 1.0 / 16, "bf16", "integer", 62, dup_every=8)
+    inp = W.generate(wl, "cpu")
+    dev = to_dev(inp)
+    ref = full_oracle(inp, wl)
+    for max_ctas in (1, 3, 0):
+        ids, toks, sc = run(dev, wl, score_kernel=TC, max_ctas=max_ctas)
+        parity.assert_exact(ref, ids, toks)
