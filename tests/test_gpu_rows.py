@@ -162,19 +162,19 @@ def test_rows_decode_262k_full_size():
 
 def test_rows_equal_scores_take_the_smallest_pools():
     """All weights zero: every eligible pool scores 0, so the row keeps its budget smallest pool
-    indices. One row's threshold bin fits the gather buffer, the other's (8,191 tied pools) does
-    not and takes the full search over the row."""
+    indices. The threshold bins of the three rows hold 1,000 and 3,000 tied pools (gathered and
+    cut in shared memory) and 8,192 (too many to gather: a search over the whole row)."""
     base = W.DECODE_TIE
-    wl = W.RowsWorkload("zero_w", (40000,), ((0, 4000), (0, 32767)), 32, 128, 4, 2048, 1.0 / 16.0, "bf16",
-                        "integer", 21)
+    wl = W.RowsWorkload("zero_w", (40000,), ((0, 4000), (0, 11999), (0, 32767)), 32, 128, 4, 2048, 1.0 / 16.0,
+                        "bf16", "integer", 21)
     inp = W.generate_rows(wl, "cuda")
     inp["w"].zero_()
     ids, toks, sc, st = _run_rows(wl, inp)
     assert st == K.KPOOL_OK
     ref = _oracle_rows(wl, inp)
     parity.assert_exact(ref, ids, toks)
-    np.testing.assert_array_equal(ids[0], np.arange(wl.budget, dtype=np.int32))
-    np.testing.assert_array_equal(ids[1], np.arange(wl.budget, dtype=np.int32))
+    for r in range(3):
+        np.testing.assert_array_equal(ids[r], np.arange(wl.budget, dtype=np.int32))
     assert base.budget == wl.budget
 
 
