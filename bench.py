@@ -50,14 +50,21 @@ FLOP_PER_PAIR_PER_HEAD_DIM = 2  # one multiply-add per (head, channel) of a scor
 # DRAM traffic of the score+select kernel from one ncu capture, per launch at the
 # pages-scale workload, tied to the kernel source it was measured on: when the
 # source hash differs the number is stale and is reported as null.
-NCU_TRAFFIC = {"kernel_sha256": "b5fcedc21cebb4c0", "workload": "pages_512k",
+NCU_TRAFFIC = {"kernel_sha256": "57046246eb85d030", "workload": "pages_512k",
                # long_128k capture: 1.101 GB read + 0.210 GB written per launch; q, w and the
                # pool ids grow with the rows, so x4 at 524288 tokens
                "bytes_per_launch": 4 * (1.100591e9 + 0.210479e9)}
 
 
 def source_sha(path: str) -> str:
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    """Hash of a CUDA source's code with comments and blank lines removed, so a comment
+    edit does not invalidate counters taken on the same code."""
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def measured_peaks() -> dict:

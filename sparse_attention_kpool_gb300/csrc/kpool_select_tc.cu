@@ -14,7 +14,8 @@
 // matrix never leaves the SM.
 //
 // Work item = 8 consecutive query rows of one sequence (the planning kernel
-// lists them deepest-first). Per item the dot products form one dense
+// lists them deepest-first; CTAs take the next one from a global counter). Per
+// item the dot products form one dense
 // contraction per tile of 128 pools:
 //   D[p, (t,h)] = kp[p,:] . q[t,h,:]     M = 128 pools, N = 8 rows x 32 heads = 256, K = 128
 // issued as 8 tcgen05.mma (K = 16 each) with bf16 operands staged by TMA in
@@ -23,23 +24,28 @@
 // heads of a query inside its own registers -- no shuffles.
 //
 // Warp roles (10 warps, one CTA per SM, persistent):
-//   warp 0      TMA producer: the item's q tile (64 KB), then pool tiles into a
-//               2-stage ring (32 KB each); a third stage measured no faster and
-//               its 32 KB buys 50% larger candidate buffers instead.
+//   warp 0      TMA producer: fetches the next work item and hands its index to
+//               the other roles through a 4-slot ring, then loads the item's q
+//               tile (64 KB) and its pool tiles into a 2-stage ring (32 KB each);
+//               a third stage measured no faster and its 32 KB buys 50% larger
+//               candidate buffers instead.
 //   warp 1      TMEM owner and MMA issuer: two 256-column accumulators, so the
 //               epilogue drains one while the tensor core fills the other.
 //   warps 2..9  epilogue, two groups of four warps; group g owns rows 4g..4g+3
 //               of every item and reads their 128 columns of every accumulator;
 //               warp w reads TMEM lanes 32*(w%4).. (the hardware rule). The
-//               groups synchronise only within themselves. tcgen05.ld -> relu,
+//               groups synchronise only within themselves. Per row: tcgen05.ld
+//               (the next row's columns and head weights load meanwhile) -> relu,
 //               |scale|*w, head sum in fp32 (packed f32x2 FMAs) -> selection key
 //               -> threshold filter -> candidate buffer in shared memory.
-// Selection: 1536 candidate slots per query row. A key enters only if it beats
-// the row's threshold. When a buffer passes 1408 entries the owning group's four
-// warps run a radix threshold search over it together and keep between budget and
-// budget+64 keys; the threshold rises to the search's edge. After the last tile
-// each row is cut to exactly `budget` keys the same way, then one warp per row
-// sorts them in registers (bitonic) and writes the ranked ids.
+// Selection: 1536 candidate slots per query row, in four 384-slot regions, one
+// per warp of the owning group, so a warp appends with a register count and no
+// atomics. A key enters only if it beats the row's threshold. When a region
+// passes 352 entries the group's four warps run a radix threshold search over the
+// row together and keep between budget and budget+64 keys, spread evenly over the
+// regions; the threshold rises to the search's edge. After the last tile each row
+// is cut to exactly `budget` keys the same way, then one warp per row sorts them
+// in registers (bitonic) and writes the ranked ids.
 //
 // Every mbarrier wait is bounded (poll count and ~1 s of wall time). A wait that
 // runs out records KPOOL_ERR_DEVICE_TIMEOUT in the workspace header; all roles
