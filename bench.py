@@ -537,41 +537,72 @@ def main():
     gated_ms = ga.elapsed_time(gb) / args.steps  # plan + gated pooling
     del gate, kp_g, gws
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers: every step copies its inputs
+    # from pinned host memory and its pool and token ids back, pipelined the way a caller
+    # would drive the library -- two device buffer sets, the next step's inputs upload on
+    # one copy stream and the previous step's results download on another while the
+    # current step computes on the main stream
     e2e = None
     if not args.no_e2e:
         h_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
         for k in h_in:
             h_in[k].copy_(inp[k])
-        d_in = {k: torch.empty_like(v) for k, v in inp.items()}
-        h_ids = torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True)
-        h_toks = torch.empty(toks.shape, dtype=toks.dtype, pin_memory=True)
+        d_in = [inp, {k: torch.empty_like(v) for k, v in inp.items()}]
+        d_ids = [ids, torch.empty_like(ids)]
+        d_toks = [toks, torch.empty_like(toks)]
+        h_ids = [torch.empty(ids.shape, dtype=ids.dtype, pin_memory=True) for _ in range(2)]
+        h_toks = [torch.empty(toks.shape, dtype=toks.dtype, pin_memory=True) for _ in range(2)]
         bi = sum(v.numel() * v.element_size() for v in h_in.values())
-        bo = h_ids.numel() * 4 + h_toks.numel() * 4
+        bo = h_ids[0].numel() * 4 + h_toks[0].numel() * 4
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        computed = [torch.cuda.Event(), torch.cuda.Event()]
+        uploaded = [torch.cuda.Event(), torch.cuda.Event()]
+        downloaded = [torch.cuda.Event(), torch.cuda.Event()]
 
-        def e2e_step():
-            for k in d_in:
-                d_in[k].copy_(h_in[k], non_blocking=True)
-            K.kpool_select_ex(d_in["q"], d_in["k"], d_in["w"], d_in["cu_seqlens"], wl.kpool, wl.index_topk,
-                              wl.scale, out_pool_ids=ids, out_token_ids=toks, workspace=ws, stream=stream)
-            h_ids.copy_(ids, non_blocking=True)
-            h_toks.copy_(toks, non_blocking=True)
+        def e2e_steps(n):
+            for i in range(n):
+                b = i & 1
+                if i >= 2:
+                    up.wait_event(computed[b])        # step i-2 is done reading these inputs
+                with torch.cuda.stream(up):
+                    for k in h_in:
+                        d_in[b][k].copy_(h_in[k], non_blocking=True)
+                    uploaded[b].record(up)
+                stream.wait_event(uploaded[b])
+                if i >= 2:
+                    stream.wait_event(downloaded[b])  # step i-2's results have left these buffers
+                K.kpool_select_ex(d_in[b]["q"], d_in[b]["k"], d_in[b]["w"], d_in[b]["cu_seqlens"], wl.kpool,
+                                  wl.index_topk, wl.scale, out_pool_ids=d_ids[b], out_token_ids=d_toks[b],
+                                  workspace=ws, stream=stream)
+                computed[b].record(stream)
+                down.wait_event(computed[b])
+                with torch.cuda.stream(down):
+                    h_ids[b].copy_(d_ids[b], non_blocking=True)
+                    h_toks[b].copy_(d_toks[b], non_blocking=True)
+                    downloaded[b].record(down)
 
-        e2e_step()
+        e2e_steps(2)
         torch.cuda.synchronize()
         barrier(world)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        e2e_steps(args.steps)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
         b.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world)
         e2e = {"value": world * pairs / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
-        del d_in, h_in
+               "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
+               "pipelining": "2 buffer sets; uploads and downloads on two copy streams overlap compute"}
+        st = K.kpool_last_device_error(ws)
+        if st != K.KPOOL_OK:
+            raise K.KpoolError(st, "device (end-to-end run)")
+        del d_in, h_in, h_ids, h_toks
 
     peaks = measured_peaks()
     peak_burst = float(peaks["bf16_tflops"])
