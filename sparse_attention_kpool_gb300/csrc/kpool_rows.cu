@@ -85,7 +85,7 @@ __device__ int block_exclusive_scan(int v, int* total, int* s_warp) {
 }
 
 // ------------------------------------------------------------------ R0 plan
-__global__ void __launch_bounds__(1024) rows_plan_kernel(const int32_t* __restrict__ cu, int S, int64_t T,
+__global__ void __launch_bounds__(256) rows_plan_kernel(const int32_t* __restrict__ cu, int S, int64_t T,
                                                          const int32_t* __restrict__ row_seq,
                                                          const int32_t* __restrict__ row_pos, int R, int kpool,
                                                          WorkspaceHeader* hdr, int32_t* pool_off, RowInfo* info,
@@ -612,7 +612,7 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.hist, 0, L.cleared_bytes, stream);
   if (e != cudaSuccess) return e;
-  rows_plan_kernel<<<1, 1024, 0, stream>>>(cu, S, T, row_seq, row_pos, R, kpool, hdr, pool_off, info, unit_off);
+  rows_plan_kernel<<<1, 256, 0, stream>>>(cu, S, T, row_seq, row_pos, R, kpool, hdr, pool_off, info, unit_off);
   e = cudaGetLastError();
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return e;
