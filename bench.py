@@ -254,8 +254,8 @@ def rows_config(wl: W.RowsWorkload, world: int) -> dict:
             f"{len(wl.seqlens)} x {wl.seqlens[0]}", "rows": wl.num_rows, "heads": wl.heads,
             "head_dim": wl.head_dim, "kpool": wl.kpool, "index_topk": wl.index_topk, "budget": wl.budget,
             "scale": wl.scale, "inputs": "k, q bf16 N(0,1), w fp32 U(0,1), seeded (CUDA Philox)",
-            "l2": "pooled keys of all rows' sequences (%.0f MiB) exceed L2" % (
-                wl.total_tokens // wl.kpool * wl.head_dim * 2 / 2**20),
+            "l2": "pooled keys of all rows' sequences (%.0f MiB) exceed L2; a 256 MiB read flushes it "
+                  "between steps" % (wl.total_tokens // wl.kpool * wl.head_dim * 2 / 2**20),
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
@@ -316,8 +316,12 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
     torch.cuda.synchronize()
     if K.kpool_last_device_error(ws) != K.KPOOL_OK:
         raise K.KpoolError(K.kpool_last_device_error(ws), "device")
-    # an L2-sized write between steps so every step reads the cache from HBM
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # a read of 256 MiB (twice L2) between steps, so every step reads the key cache from
+    # HBM; a read leaves no dirty lines whose write-back would land in the next step
+    flush = torch.ones(64 << 20, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        return flush.max()
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
@@ -325,7 +329,7 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
     torch.cuda.synchronize()
     per_step = []
     for s_i in range(args.steps):
-        flush.fill_(s_i & 0xFF)
+        flush_l2()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -337,19 +341,26 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
     ms = statistics.median([a.elapsed_time(b) for a, b in per_step])
     # the same step captured once in a CUDA graph and replayed (what a decode loop would do)
     graph_ms = None
+    k_ms_graph = None
     try:
         gs = torch.cuda.Stream()
         gs.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
+        g_ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in g_ev:
+            e.record(stream)
+        # `graph` is the step a decode loop replays; `graph_ev` the same step with the stage
+        # events as event-record nodes (they lengthen the graph), for the per-kernel times
+        graph, graph_ev = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.stream(gs):
-            with torch.cuda.graph(graph, stream=gs):
-                K.kpool_select_rows(inp["q"], inp["w"], inp["row_seq"], inp["row_pos"], kp, inp["cu_seqlens"],
-                                    wl.total_tokens, wl.kpool, wl.index_topk, wl.scale, out_pool_ids=ids,
-                                    out_token_ids=toks, workspace=ws, stream=gs)
+            for g, evs in ((graph, None), (graph_ev, g_ev)):
+                with torch.cuda.graph(g, stream=gs):
+                    K.kpool_select_rows(inp["q"], inp["w"], inp["row_seq"], inp["row_pos"], kp, inp["cu_seqlens"],
+                                        wl.total_tokens, wl.kpool, wl.index_topk, wl.scale, out_pool_ids=ids,
+                                        out_token_ids=toks, workspace=ws, stream=gs, stage_events=evs)
         stream.wait_stream(gs)
         g_t = []
         for s_i in range(args.warmup + args.steps):
-            flush.fill_(s_i & 0xFF)
+            flush_l2()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -358,10 +369,20 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
             g_t.append((a, b))
         torch.cuda.synchronize()
         graph_ms = statistics.median([a.elapsed_time(b) for a, b in g_t[args.warmup:]])
+        # per-kernel times from the graph's own event nodes (no host launch gaps): one
+        # replay at a time, its stage events read before the next replay records them again
+        g_k = []
+        for s_i in range(args.steps):
+            flush_l2()
+            graph_ev.replay()
+            torch.cuda.synchronize()
+            g_k.append([g_ev[i].elapsed_time(g_ev[i + 1]) for i in range(3)])
+        k_ms_graph = [statistics.median([x[i] for x in g_k]) for i in range(3)]
     except RuntimeError as ex:  # graph capture unavailable: report the eager number only
         print(f"graph capture skipped: {ex}", file=sys.stderr)
     ms_step = max_over_ranks(ms, world)
-    k_ms = [statistics.median([evs[i].elapsed_time(evs[i + 1]) for evs in step_events]) for i in range(3)]
+    k_ms_eager = [statistics.median([evs[i].elapsed_time(evs[i + 1]) for evs in step_events]) for i in range(3)]
+    k_ms = k_ms_graph if k_ms_graph is not None else k_ms_eager
     pairs = wl.scored_pairs()
     value = world * pairs / (ms_step / 1e3)
     # e2e: the rows' inputs come from pinned host memory, the selection goes back to it
@@ -375,7 +396,7 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
     bo = h_ids.numel() * 4 + h_toks.numel() * 4
     e2e_t = []
     for _ in range(args.warmup + args.steps):
-        flush.fill_(1)
+        flush_l2()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -399,7 +420,9 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": rows_config(wl, world),
         "us_per_decode_step": 1e3 * ms_step,
         "us_per_decode_step_graph": None if graph_ms is None else 1e3 * graph_ms,
-        "kernel_ms": {"plan": k_ms[0], "score": k_ms[1], "select": k_ms[2]},
+        "kernel_ms": {"plan": k_ms[0], "score": k_ms[1], "select": k_ms[2],
+                      "timed": "graph replay" if k_ms_graph is not None else "eager"},
+        "kernel_ms_eager": {"plan": k_ms_eager[0], "score": k_ms_eager[1], "select": k_ms_eager[2]},
         "roofline": {"kernel": "rows_score_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                      "peak_kind": f"HBM copy, {peaks['_source']}", "algorithmic_bytes_per_launch": score_bytes},

@@ -88,7 +88,9 @@ typedef struct {
   void* const* stage_events;  /* NULL, or 5 cudaEvent_t (created by the caller) that are
                                  recorded on `stream` before the planning kernel and after
                                  the plan, pool, score+select and expand kernels, so a
-                                 caller can time each kernel without a profiler */
+                                 caller can time each kernel without a profiler; inside a
+                                 stream capture they become event-record nodes of the
+                                 graph, recorded again on every replay */
   int32_t reserved[4];        /* must be zero */
 } kpool_options;
 
@@ -215,7 +217,8 @@ kpool_status kpool_select_rows(const void* q, const float* w, const int32_t* row
  * kpool_select_rows with options (NULL = defaults). score_kernel must be
  * KPOOL_SCORE_AUTO; max_ctas > 0 caps the score kernel's grid (CTAs); stage_events, when
  * not NULL, holds 4 cudaEvent_t recorded on `stream` before the planning kernel
- * and after the planning, score and select kernels.
+ * and after the planning, score and select kernels (event-record nodes when the
+ * stream is being captured into a graph).
  */
 kpool_status kpool_select_rows_ex(const void* q, const float* w, const int32_t* row_seq, const int32_t* row_pos,
                                   int32_t num_rows, const void* pooled_keys, const int32_t* cu_seqlens,

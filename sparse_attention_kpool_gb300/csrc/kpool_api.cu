@@ -148,7 +148,7 @@ kpool_status select_impl(const void* q, const void* k, const void* pooled_in, co
 
   void* const* ev = opt.stage_events;
   auto mark = [&](int i) {
-    return ev == nullptr || cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), stream));
+    return ev == nullptr || cuda_ok(record_stage_event(ev[i], stream));
   };
   if (!mark(0)) return KPOOL_ERR_CUDA;
   if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, T, kpool, ws, L, stream)) || !mark(1)) return KPOOL_ERR_CUDA;

@@ -92,6 +92,18 @@ __device__ __forceinline__ void record_error(WorkspaceHeader* hdr, int code) {
   atomicCAS(&hdr->error, 0, code);
 }
 
+// Records a caller's stage event on `stream`. Inside a stream capture it is added
+// as an event-record node (cudaEventRecordExternal), so a replayed graph records it
+// on every replay and the stage times can be read from graph launches too.
+inline cudaError_t record_stage_event(void* ev, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), stream, cudaEventRecordExternal)
+             : cudaEventRecord(static_cast<cudaEvent_t>(ev), stream);
+}
+
 // ------------------------------------------------------ launch wrappers
 // Each returns cudaGetLastError() after enqueueing its kernel on `stream`.
 

@@ -41,15 +41,18 @@ constexpr int kRowsHeads = 32;
 constexpr int kRowsDim = 128;
 constexpr int kUnitPools = 128;        // pools per work unit of R1 (the split granularity)
 constexpr int kScoreWarps = 8;         // R1: 8 warps x 16 pools per round
-constexpr int kSelectThreads = 256;    // R3
-constexpr int kRowsMaxBudget = 512;    // R3 sorts at most 512 keys in one warp
+constexpr int kSelectThreads = 256;    // R3 (block_sort512_desc takes exactly 256 threads)
+constexpr int kRowsMaxBudget = 512;    // R3 sorts at most 512 keys
 constexpr int kHistBits = 12;          // histogram of score_order_bits >> (32 - kHistBits)
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kTieCap = 4096;          // pools of the threshold bin R3 can finish in shared memory
+static_assert(kTieCap >= 1024, "R3 sorts in the tie buffer (1024 keys)");
 constexpr int kCollectPools = 2048;    // R2: pools per CTA and round
 constexpr int kCollectTies = 2048;     // R2: threshold-bin pools one round can hold
 constexpr int kCollectCtasPerRow = 64; // R2: grid width; CTAs loop over a row's slices
 constexpr int kCollectThreads = 256;
+constexpr int kCollectPer = kCollectPools / kCollectThreads;  // R2: scores per thread and round
+static_assert(kCollectPer % 4 == 0, "R2 loads its scores 4 at a time");
 
 struct RowInfo {
   int32_t pool_base;  // global pooled-key row of the sequence's pool 0
@@ -301,14 +304,24 @@ __global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
 __device__ __forceinline__ void threshold_bin(const uint32_t* __restrict__ h, int budget, int* s_warp,
                                               int* out_bin, int* out_above) {
   constexpr int kPer = kHistBins / kCollectThreads;  // bins per thread, descending
+  static_assert(kPer == 16, "four 16-byte loads per thread");
   const int tid = threadIdx.x;
+  // thread t holds bins 4095 - 16 t down to 4080 - 16 t: cnt[i] is bin 4095 - 16 t - i
+  const uint4* h4 = reinterpret_cast<const uint4*>(h + kHistBins - kPer * (tid + 1));
+  uint4 v[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = h4[j];
   uint32_t cnt[kPer];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    cnt[15 - 4 * j] = v[j].x;
+    cnt[14 - 4 * j] = v[j].y;
+    cnt[13 - 4 * j] = v[j].z;
+    cnt[12 - 4 * j] = v[j].w;
+  }
   int tot = 0;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    cnt[i] = h[kHistBins - 1 - (kPer * tid + i)];
-    tot += int(cnt[i]);
-  }
+  for (int i = 0; i < kPer; ++i) tot += int(cnt[i]);
   int all;
   const int before = block_exclusive_scan(tot, &all, s_warp);
   if (before < budget && before + tot >= budget) {
@@ -345,16 +358,27 @@ __global__ void __launch_bounds__(kCollectThreads) rows_collect_kernel(
     }
     __syncthreads();
     const int p_hi = min(e, p_lo + kCollectPools);
-    // gather this slice's pools above / inside the threshold bin in shared memory (whole
-    // warps iterate together for the warp votes)
-    for (int p = p_lo + threadIdx.x; p < p_lo + ((p_hi - p_lo + 31) & ~31); p += kCollectThreads) {
-      float s = 0.0f;
-      uint32_t bin = 0;
+    // gather this slice's pools above / inside the threshold bin in shared memory: the
+    // thread's 8 consecutive scores come in two 16-byte loads (a row's stride is a
+    // multiple of 4 floats, so a load that starts below e stays inside the row)
+    const int p0 = p_lo + kCollectPer * threadIdx.x;
+    float sv[kCollectPer];
+#pragma unroll
+    for (int j = 0; j < kCollectPer / 4; ++j) {
+      float4 f = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (p0 + 4 * j < p_hi) f = *reinterpret_cast<const float4*>(row + p0 + 4 * j);
+      sv[4 * j] = f.x;
+      sv[4 * j + 1] = f.y;
+      sv[4 * j + 2] = f.z;
+      sv[4 * j + 3] = f.w;
+    }
+    // whole warps vote together on each of the eight
+#pragma unroll
+    for (int i = 0; i < kCollectPer; ++i) {
+      const int p = p0 + i;
+      const float s = sv[i];
       const bool in = p < p_hi;
-      if (in) {
-        s = row[p];
-        bin = score_order_bits(s) >> (32 - kHistBits);
-      }
+      const uint32_t bin = score_order_bits(s) >> (32 - kHistBits);
       const bool above = in && bin > thr, tie = in && bin == thr;
       const unsigned ma = __ballot_sync(0xffffffffu, above), mt = __ballot_sync(0xffffffffu, tie);
       int base_a = 0, base_t = 0;
@@ -408,7 +432,12 @@ __global__ void __launch_bounds__(kSelectThreads) rows_select_kernel(
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const int width = budget * kpool + kpool;
   int32_t* tok = out_tokens + int64_t(r) * width;
-  const RowInfo ri = hdr->n_levels != 0 ? info[r] : RowInfo{0, -1, 0, 0};
+  // the row record and both gather counts in one round of loads (without valid
+  // cu_seqlens the record is never read)
+  const int n_levels = hdr->n_levels;
+  const RowInfo ri_raw = info[r];
+  const int cnt_above = cand_cnt[r], cnt_tie = tie_cnt[r];
+  const RowInfo ri = n_levels != 0 ? ri_raw : RowInfo{0, -1, 0, 0};
   if (ri.e < 0) {  // malformed cu_seqlens or an invalid row: every slot empty
     for (int s = tid; s < width; s += kSelectThreads) tok[s] = -1;
     for (int j = tid; j < budget; j += kSelectThreads) {
@@ -424,14 +453,22 @@ __global__ void __launch_bounds__(kSelectThreads) rows_select_kernel(
   for (int j = tid; j < kRowsMaxBudget; j += kSelectThreads) s_keys[j] = 0ull;
   __syncthreads();
 
-  const int n_above = e > budget ? cand_cnt[r] : 0, n_tie = e > budget ? tie_cnt[r] : 0;
+  const int n_above = e > budget ? cnt_above : 0, n_tie = e > budget ? cnt_tie : 0;
   if (e <= budget) {
     for (int p = tid; p < e; p += kSelectThreads) s_keys[p] = make_key(row[p], uint32_t(p));
   } else if (budget > 0 && n_tie <= kTieCap) {
     // R2 gathered the n_above pools above the threshold bin and the n_tie pools in it:
     // keep the first, and the top budget - n_above of the second by full key
-    for (int j = tid; j < n_above; j += kSelectThreads) s_keys[j] = cand[int64_t(r) * kRowsMaxBudget + j];
-    for (int j = tid; j < n_tie; j += kSelectThreads) s_ties[j] = ties[int64_t(r) * kTieCap + j];
+#pragma unroll
+    for (int i = 0; i < kRowsMaxBudget / kSelectThreads; ++i) {
+      const int j = tid + i * kSelectThreads;
+      if (j < n_above) s_keys[j] = cand[int64_t(r) * kRowsMaxBudget + j];
+    }
+#pragma unroll
+    for (int i = 0; i < kTieCap / kSelectThreads; ++i) {
+      const int j = tid + i * kSelectThreads;
+      if (j < n_tie) s_ties[j] = ties[int64_t(r) * kTieCap + j];
+    }
     __syncthreads();
     const int need = budget - n_above;
     if (n_tie > need) {
@@ -523,20 +560,22 @@ __global__ void __launch_bounds__(kSelectThreads) rows_select_kernel(
     }
   }
   __syncthreads();
-  if (tid < 32) {
-    uint64_t k[16];
+  {
+    // the whole block ranks the (at most 512) kept keys; s_ties is free by now
+    const int warp = tid >> 5;
+    uint64_t k[2];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) k[j] = s_keys[32 * j + lane];
-    warp_sort512_blocked_desc(k);  // lane l holds ranks 16 l .. 16 l + 15
+    for (int h = 0; h < 2; ++h) k[h] = s_keys[64 * warp + 32 * h + lane];
+    block_sort512_desc(k, s_ties);  // k[h] is now rank 64 warp + 32 h + lane
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int rank = 16 * lane + j;
+    for (int h = 0; h < 2; ++h) {
+      const int rank = 64 * warp + 32 * h + lane;
       if (rank < budget) {
-        const bool has = rank < m && k[j] != 0ull;
-        const int32_t id = has ? int32_t(key_pool(k[j])) : -1;
+        const bool has = rank < m && k[h] != 0ull;
+        const int32_t id = has ? int32_t(key_pool(k[h])) : -1;
         s_ids[rank] = id;
         out_ids[int64_t(r) * budget + rank] = id;
-        if (out_scores) out_scores[int64_t(r) * budget + rank] = has ? key_score(k[j]) : -INFINITY;
+        if (out_scores) out_scores[int64_t(r) * budget + rank] = has ? key_score(k[h]) : -INFINITY;
       }
     }
   }
@@ -607,7 +646,7 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
   uint64_t* ties = reinterpret_cast<uint64_t*>(ws + L.ties);
   auto mark = [&](int i) {
     return stage_events == nullptr ? cudaSuccess
-                                   : cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), stream);
+                                   : record_stage_event(stage_events[i], stream);
   };
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.hist, 0, L.cleared_bytes, stream);

@@ -132,97 +132,13 @@ __device__ inline int warp_select_compact(uint64_t* buf, int n, int budget, int 
   return base;
 }
 
-// Descending bitonic sort of 32 * kSlots keys held in registers, one warp.
-// Key index i = 32 * r + lane (k[r] of lane `lane`), so loads and stores of a
-// buffer are coalesced: strides below 32 exchange with another lane through
-// shuffles, larger strides swap registers of the same lane.
-template <int kSlots>
-__device__ __forceinline__ void warp_sort_regs_desc(uint64_t (&k)[kSlots]) {
-  constexpr int kN = 32 * kSlots;
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int size = 2; size <= kN; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride >= 32) {
-        const int rs = stride >> 5;
-#pragma unroll
-        for (int r = 0; r < kSlots; ++r) {
-          if ((r & rs) == 0) {
-            const int r2 = r | rs;
-            const bool desc = ((32 * r) & size) == 0;
-            const uint64_t a = k[r], b = k[r2];
-            const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-            k[r] = desc ? hi : lo;
-            k[r2] = desc ? lo : hi;
-          }
-        }
-      } else {
-        const bool lower = (lane & stride) == 0;
-#pragma unroll
-        for (int r = 0; r < kSlots; ++r) {
-          const uint64_t other = __shfl_xor_sync(0xffffffffu, k[r], stride);
-          const bool desc = ((32 * r + lane) & size) == 0;
-          const bool take_max = lower == desc;
-          const uint64_t hi = k[r] > other ? k[r] : other, lo = k[r] > other ? other : k[r];
-          k[r] = take_max ? hi : lo;
-        }
-      }
-    }
-  }
+// Compare-exchange of a bitonic network on 64-bit keys: returns the key this
+// position keeps, the larger of (mine, other) when keep_max, else the smaller.
+__device__ __forceinline__ uint64_t bitonic_keep(uint64_t mine, uint64_t other, bool keep_max) {
+  return (mine > other) == keep_max ? mine : other;
 }
 
-// One register stage of warp_sort_regs_desc_rolled: pairs (r, r | RS) of the same lane.
-template <int RS, int kSlots>
-__device__ __forceinline__ void sort_reg_stage(uint64_t (&k)[kSlots], int size) {
-#pragma unroll
-  for (int r = 0; r < kSlots; ++r) {
-    if ((r & RS) == 0) {
-      const int r2 = r | RS;
-      const bool desc = ((32 * r) & size) == 0;
-      const uint64_t a = k[r], b = k[r2];
-      const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-      k[r] = desc ? hi : lo;
-      k[r2] = desc ? lo : hi;
-    }
-  }
-}
-
-// Same network as warp_sort_regs_desc for 512 keys (16 per lane), with the stage
-// loops kept rolled so the code stays small (it runs once per row and item).
-__device__ __forceinline__ void warp_sort512_regs_desc(uint64_t (&k)[16]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int size = 2; size <= 512; size <<= 1) {
-#pragma unroll 1
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride >= 32) {
-        switch (stride >> 5) {
-          case 1: sort_reg_stage<1>(k, size); break;
-          case 2: sort_reg_stage<2>(k, size); break;
-          case 4: sort_reg_stage<4>(k, size); break;
-          default: sort_reg_stage<8>(k, size); break;
-        }
-      } else {
-        const bool lower = (lane & stride) == 0;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const uint64_t other = __shfl_xor_sync(0xffffffffu, k[r], stride);
-          const bool desc = ((32 * r + lane) & size) == 0;
-          const uint64_t hi = k[r] > other ? k[r] : other, lo = k[r] > other ? other : k[r];
-          k[r] = lower == desc ? hi : lo;
-        }
-      }
-    }
-  }
-}
-
-// Blocked-layout variant: key index i = 16 * lane + r (k[r] of lane `lane`).
-// Strides below 16 pair registers of the same lane (30 of the 45 stages), larger
-// strides exchange with lane ^ (stride / 16) through shuffles (15 stages). The
-// starting placement of the keys does not matter to a sorting network, so callers
-// load them striped (conflict-free) and read the result as blocked: lane l ends
-// up holding ranks 16 l .. 16 l + 15.
+// One in-register stage of warp_sort512_blocked_desc: pairs (r, r | RS) of a lane.
 template <int RS>
 __device__ __forceinline__ void sort_blocked_reg_stage(uint64_t (&k)[16], int size, int lane) {
 #pragma unroll
@@ -238,6 +154,14 @@ __device__ __forceinline__ void sort_blocked_reg_stage(uint64_t (&k)[16], int si
   }
 }
 
+// Descending bitonic sort of 512 keys in one warp, blocked layout: key index
+// i = 16 * lane + r (k[r] of lane `lane`). Strides below 16 pair registers of the
+// same lane (30 of the 45 stages), larger strides exchange with lane ^ (stride / 16)
+// through shuffles (15 stages). The starting placement of the keys does not matter
+// to a sorting network, so callers load them striped (conflict-free) and read the
+// result as blocked: lane l ends up holding ranks 16 l .. 16 l + 15. The stage loops
+// stay rolled: fully unrolled, the sort alone runs about 30 % faster, but the score
+// kernel that calls it once per row and item loses more than that in its main loop.
 __device__ __forceinline__ void warp_sort512_blocked_desc(uint64_t (&k)[16]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
@@ -259,6 +183,47 @@ __device__ __forceinline__ void warp_sort512_blocked_desc(uint64_t (&k)[16]) {
           const uint64_t other = __shfl_xor_sync(0xffffffffu, k[r], ls);
           const uint64_t hi = k[r] > other ? k[r] : other, lo = k[r] > other ? other : k[r];
           k[r] = take_max ? hi : lo;
+        }
+      }
+    }
+  }
+}
+
+// Descending bitonic sort of 512 keys by a whole block of 256 threads: k[h] of
+// thread (warp w, lane l) is key 64 w + 32 h + l. Strides up to 16 go through
+// shuffles, stride 32 swaps the thread's two keys, strides 64..256 cross warps
+// through s_buf (1024 keys of shared memory, two alternating halves, so each such
+// stage needs one barrier). On return the thread holds ranks 64 w + 32 h + l.
+__device__ __forceinline__ void block_sort512_desc(uint64_t (&k)[2], uint64_t* s_buf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int half = 0;
+#pragma unroll
+  for (int size = 2; size <= 512; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 64) {
+        uint64_t* b = s_buf + 512 * half;
+        half ^= 1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) b[64 * warp + 32 * h + lane] = k[h];
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = 64 * warp + 32 * h + lane;
+          k[h] = bitonic_keep(k[h], b[i ^ stride], ((i & stride) == 0) == ((i & size) == 0));
+        }
+      } else if (stride == 32) {
+        const bool desc = ((64 * warp + lane) & size) == 0;
+        const uint64_t a = k[0], c = k[1];
+        const bool swap = (a > c) != desc;
+        k[0] = swap ? c : a;
+        k[1] = swap ? a : c;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = 64 * warp + 32 * h + lane;
+          k[h] = bitonic_keep(k[h], __shfl_xor_sync(0xffffffffu, k[h], stride),
+                              ((i & stride) == 0) == ((i & size) == 0));
         }
       }
     }
