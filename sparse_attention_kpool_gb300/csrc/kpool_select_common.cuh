@@ -138,52 +138,38 @@ __device__ __forceinline__ uint64_t bitonic_keep(uint64_t mine, uint64_t other, 
   return (mine > other) == keep_max ? mine : other;
 }
 
-// One in-register stage of warp_sort512_blocked_desc: pairs (r, r | RS) of a lane.
-template <int RS>
-__device__ __forceinline__ void sort_blocked_reg_stage(uint64_t (&k)[16], int size, int lane) {
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if ((r & RS) == 0) {
-      const int r2 = r | RS;
-      const bool desc = ((16 * lane + r) & size) == 0;
-      const uint64_t a = k[r], b = k[r2];
-      const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-      k[r] = desc ? hi : lo;
-      k[r2] = desc ? lo : hi;
-    }
-  }
-}
-
 // Descending bitonic sort of 512 keys in one warp, blocked layout: key index
 // i = 16 * lane + r (k[r] of lane `lane`). Strides below 16 pair registers of the
 // same lane (30 of the 45 stages), larger strides exchange with lane ^ (stride / 16)
 // through shuffles (15 stages). The starting placement of the keys does not matter
 // to a sorting network, so callers load them striped (conflict-free) and read the
-// result as blocked: lane l ends up holding ranks 16 l .. 16 l + 15. The stage loops
-// stay rolled: fully unrolled, the sort alone runs about 30 % faster, but the score
-// kernel that calls it once per row and item loses more than that in its main loop.
+// result as blocked: lane l ends up holding ranks 16 l .. 16 l + 15. Every stage is
+// unrolled (with rolled stage loops a lone warp spends a third more time on loop
+// control and reconvergence); a caller whose own code is register-hungry keeps the
+// network out of line so its allocation does not depend on this one.
 __device__ __forceinline__ void warp_sort512_blocked_desc(uint64_t (&k)[16]) {
   const int lane = threadIdx.x & 31;
-#pragma unroll 1
+#pragma unroll
   for (int size = 2; size <= 512; size <<= 1) {
-#pragma unroll 1
+#pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       if (stride < 16) {
-        switch (stride) {
-          case 1: sort_blocked_reg_stage<1>(k, size, lane); break;
-          case 2: sort_blocked_reg_stage<2>(k, size, lane); break;
-          case 4: sort_blocked_reg_stage<4>(k, size, lane); break;
-          default: sort_blocked_reg_stage<8>(k, size, lane); break;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          if ((r & stride) == 0) {
+            const int r2 = r | stride;
+            const bool desc = ((16 * lane + r) & size) == 0;
+            const uint64_t a = k[r], c = k[r2];
+            const bool swap = (a > c) != desc;
+            k[r] = swap ? c : a;
+            k[r2] = swap ? a : c;
+          }
         }
       } else {
         const int ls = stride >> 4;
-        const bool take_max = ((lane & ls) == 0) == (((16 * lane) & size) == 0);
+        const bool keep_max = ((lane & ls) == 0) == (((16 * lane) & size) == 0);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const uint64_t other = __shfl_xor_sync(0xffffffffu, k[r], ls);
-          const uint64_t hi = k[r] > other ? k[r] : other, lo = k[r] > other ? other : k[r];
-          k[r] = take_max ? hi : lo;
-        }
+        for (int r = 0; r < 16; ++r) k[r] = bitonic_keep(k[r], __shfl_xor_sync(0xffffffffu, k[r], ls), keep_max);
       }
     }
   }

@@ -200,6 +200,46 @@ __device__ __forceinline__ Item load_item(const int2* items, const int32_t* cu, 
   return m;
 }
 
+// Final ranking of one row by one warp: its candidates (at most kFinalChunk per
+// region, at most budget in all) sorted, then the first `budget` ranks written as
+// pool ids (-1 for empty slots) and, when sc_row is given, scores (-inf). Kept out of
+// line: inlined, the unrolled sort network changes the register allocation of the
+// scoring loop around it, which then runs slower than the sort gains.
+__device__ __noinline__ void rank_and_write_row(const uint64_t* buf, const int32_t* c, int budget, int32_t* ids_row,
+                                                float* sc_row) {
+  const int lane = threadIdx.x & 31;
+  uint64_t kk[kMaxBudget / 32];
+#pragma unroll
+  for (int j = 0; j < kMaxBudget / 32; ++j) {
+    constexpr int kPerRegion = kFinalChunk / 32;
+    const int r = j / kPerRegion, off = (j % kPerRegion) * 32 + lane;  // region, offset
+    kk[j] = off < c[r] ? buf[r * kReg + off] : 0ull;
+  }
+  warp_sort512_blocked_desc(kk);  // lane l now holds ranks 16 l .. 16 l + 15
+  const int o0 = 16 * lane;
+  if (o0 + 16 <= budget && (reinterpret_cast<uintptr_t>(ids_row + o0) & 15u) == 0) {  // 16-byte vector stores
+    int4* dst = reinterpret_cast<int4*>(ids_row + o0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int4 v;
+      v.x = kk[4 * j + 0] ? int32_t(key_pool(kk[4 * j + 0])) : -1;
+      v.y = kk[4 * j + 1] ? int32_t(key_pool(kk[4 * j + 1])) : -1;
+      v.z = kk[4 * j + 2] ? int32_t(key_pool(kk[4 * j + 2])) : -1;
+      v.w = kk[4 * j + 3] ? int32_t(key_pool(kk[4 * j + 3])) : -1;
+      dst[j] = v;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (o0 + j < budget) ids_row[o0 + j] = kk[j] ? int32_t(key_pool(kk[j])) : -1;
+  }
+  if (sc_row) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (o0 + j < budget) sc_row[o0 + j] = kk[j] ? key_score(kk[j]) : -INFINITY;
+  }
+}
+
 template <bool kNegScale>
 __global__ void __launch_bounds__(kThreads, 1)
     select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
@@ -582,40 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = rbase + wq;
         const int row = it.t0 + q;
         if (row < it.len) {
-          const uint64_t* buf = s_cand + q * kCap;
-          const int32_t* c = s_count + q * 4;
-          uint64_t kk[kMaxBudget / 32];
-#pragma unroll
-          for (int j = 0; j < kMaxBudget / 32; ++j) {
-            constexpr int kPerRegion = kFinalChunk / 32;
-            const int r = j / kPerRegion, off = (j % kPerRegion) * 32 + lane;  // region, offset
-            kk[j] = off < c[r] ? buf[r * kReg + off] : 0ull;
-          }
-          warp_sort512_blocked_desc(kk);  // lane l now holds ranks 16 l .. 16 l + 15
           const int64_t grow = it.seq_start + row;
-          const int o0 = 16 * lane;
-          int32_t* dst_row = out_ids + grow * budget + o0;
-          if (o0 + 16 <= budget && (reinterpret_cast<uintptr_t>(dst_row) & 15u) == 0) {  // 16-byte vector stores
-            int4* dst = reinterpret_cast<int4*>(dst_row);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              int4 v;
-              v.x = kk[4 * j + 0] ? int32_t(key_pool(kk[4 * j + 0])) : -1;
-              v.y = kk[4 * j + 1] ? int32_t(key_pool(kk[4 * j + 1])) : -1;
-              v.z = kk[4 * j + 2] ? int32_t(key_pool(kk[4 * j + 2])) : -1;
-              v.w = kk[4 * j + 3] ? int32_t(key_pool(kk[4 * j + 3])) : -1;
-              dst[j] = v;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (o0 + j < budget) out_ids[grow * budget + o0 + j] = kk[j] ? int32_t(key_pool(kk[j])) : -1;
-          }
-          if (out_scores) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (o0 + j < budget) out_scores[grow * budget + o0 + j] = kk[j] ? key_score(kk[j]) : -INFINITY;
-          }
+          rank_and_write_row(s_cand + q * kCap, s_count + q * 4, budget, out_ids + grow * budget,
+                             out_scores ? out_scores + grow * budget : nullptr);
           __syncwarp();
         }
       }
