@@ -200,6 +200,23 @@ __device__ __forceinline__ Item load_item(const int2* items, const int32_t* cu, 
   return m;
 }
 
+// Cooperative compaction of one row's candidates by the epilogue group's four warps
+// (thread gt of 128, named barrier bar_id): keeps between budget and budget + slack
+// keys (exactly budget for slack 0), dealt evenly back over the four regions, whose
+// counts cnt4[0..3] it updates. With `tau`, thread 0 stores the new admission bound
+// (edge - 1: from now on a key must reach the edge to matter). Kept out of line:
+// inlined, its code costs the scoring loop around it 3-4 % (register allocation).
+__device__ __noinline__ void compact_row(uint64_t* buf, int32_t* cnt4, int budget, int slack, int gt, int bar_id,
+                                         SelectScratch* sel, uint64_t* tau) {
+  using L = QuarteredLayout<kReg>;
+  const int32_t* c = cnt4;
+  uint64_t edge;
+  const int kept = block_select_compact_in<kCap / 128, 4>(buf, c[0] + c[1] + c[2] + c[3], budget, slack, gt, bar_id,
+                                                         sel, &edge, L{c});
+  if (gt < 4) cnt4[gt] = L::region_count(kept, gt);  // block_select_compact_in ends with a group barrier
+  if (tau != nullptr && gt == 0) *tau = edge - 1;
+}
+
 // Final ranking of one row by one warp: its candidates (at most kFinalChunk per
 // region, at most budget in all) sorted, then the first `budget` ranks written as
 // pool ids (-1 for empty slots) and, when sc_row is given, scores (-inf). Kept out of
@@ -584,12 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q = rbase + j;
             const int32_t* c = s_count + q * 4;
             if (max(max(c[0], c[1]), max(c[2], c[3])) > kRegMark) {
-              uint64_t edge;
-              using L = QuarteredLayout<kReg>;
-              const int kept = block_select_compact_in<kCap / 128, 4>(
-                  s_cand + q * kCap, c[0] + c[1] + c[2] + c[3], budget, kSlack, gt, bar_id, sel, &edge, L{c});
-              if (gt < 4) s_count[q * 4 + gt] = L::region_count(kept, gt);
-              if (gt == 0) s_tau[q] = edge - 1;  // a key must reach the edge to matter from now on
+              compact_row(s_cand + q * kCap, s_count + q * 4, budget, kSlack, gt, bar_id, sel, s_tau + q);
             }
           }
           named_bar(bar_id, 128);
@@ -610,11 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = c[0] + c[1] + c[2] + c[3];
         // the sort below reads the first kFinalChunk slots of each region
         if (n > budget || max(max(c[0], c[1]), max(c[2], c[3])) > kFinalChunk) {
-          using L = QuarteredLayout<kReg>;
-          uint64_t edge;
-          const int kept = block_select_compact_in<kCap / 128, 4>(s_cand + q * kCap, n, budget, 0, gt, bar_id, sel,
-                                                                 &edge, L{c});
-          if (gt < 4) s_count[q * 4 + gt] = L::region_count(kept, gt);
+          compact_row(s_cand + q * kCap, s_count + q * 4, budget, 0, gt, bar_id, sel, nullptr);
         }
       }
       named_bar(bar_id, 128);
