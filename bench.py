@@ -50,10 +50,10 @@ FLOP_PER_PAIR_PER_HEAD_DIM = 2  # one multiply-add per (head, channel) of a scor
 # DRAM traffic of the score+select kernel from one ncu capture, per launch at the
 # pages-scale workload, tied to the kernel source it was measured on: when the
 # source hash differs the number is stale and is reported as null.
-NCU_TRAFFIC = {"kernel_sha256": "d34f19d41998171f", "workload": "pages_512k",
-               # long_128k capture: 1.102 GB read + 0.213 GB written per launch; q, w and the
+NCU_TRAFFIC = {"kernel_sha256": "dddbed140292a189", "workload": "pages_512k",
+               # long_128k capture: 1.103 GB read + 0.214 GB written per launch; q, w and the
                # pool ids grow with the rows, so x4 at 524288 tokens
-               "bytes_per_launch": 4 * (1.101545e9 + 0.213124e9)}
+               "bytes_per_launch": 4 * (1.103136e9 + 0.213674e9)}
 
 
 def source_sha(path: str) -> str:

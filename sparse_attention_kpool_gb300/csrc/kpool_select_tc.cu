@@ -257,6 +257,153 @@ __device__ __noinline__ void rank_and_write_row(const uint64_t* buf, const int32
   }
 }
 
+// Producer (one thread of warp 0): takes work items from the global counter and
+// hands them to the MMA issuer and the epilogue through the ring, then streams each
+// item's query block and pool tiles into shared memory with TMA. The two warp roles
+// that run on a single thread are separate functions so the epilogue's code (the
+// kernel body) is allocated on its own.
+__device__ __noinline__ void producer_role(const CUtensorMap* tmap_q, const CUtensorMap* tmap_kp, const int32_t* cu,
+                                           const int32_t* pool_off, const int2* items, WorkspaceHeader* hdr, int kpool,
+                                           int n_items) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Bars bar = bars_at(smem);
+  volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + kOffMisc + 4);
+  volatile int32_t* s_ring = reinterpret_cast<volatile int32_t*>(smem + kOffRing);
+  const uint64_t pol_q = ptx::policy_evict_first();
+  const uint64_t pol_kp = ptx::policy_evict_last();
+  int stage = 0;
+  uint32_t phase = 0, q_phase = 0;
+  uint32_t fills = 0;  // pool-tile fills armed so far (stage = fill index mod kStages)
+  uint32_t q_armed = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    // next work item from the global counter (heaviest first, as the plan sorted
+    // them), handed to the MMA issuer and the epilogue through the ring
+    const int slot = r % kRing;
+    const uint32_t use = uint32_t(r / kRing);
+    if (use > 0 && !ptx::mbar_wait_bounded(bar.ring_empty + slot, (use - 1) & 1, kMaxPolls, kMaxWaitNs,
+                                           kBackoffNs)) {
+      ok = false;
+      break;
+    }
+    int idx = atomicAdd(&hdr->next_item, 1);
+    if (idx >= n_items) idx = -1;
+    s_ring[slot] = idx;
+    ptx::mbar_arrive(bar.ring_full + slot);
+    if (idx < 0) break;
+    const Item it = load_item(items, cu, pool_off, idx, kpool);
+    if (it.n_tiles == 0) continue;
+    if (!ptx::mbar_wait_bounded(bar.q_empty, q_phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
+      ok = false;
+      break;
+    }
+    q_phase ^= 1;
+    uint8_t* qdst = smem + kOffQ;
+    const int32_t qrow = int32_t((it.seq_start + it.t0) * kHeads);
+    ptx::mbar_arrive_expect_tx(bar.q_full, kQBytes);
+    ptx::tma_load_2d_hint(qdst, tmap_q, bar.q_full, 0, qrow, pol_q);
+    ptx::tma_load_2d_hint(qdst + kQHalfBytes, tmap_q, bar.q_full, 64, qrow, pol_q);
+    ++q_armed;
+    for (int i = 0; i < it.n_tiles; ++i) {
+      if (!ptx::mbar_wait_bounded(bar.empty + stage, phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) ||
+          *abort_flag) {
+        ok = false;
+        break;
+      }
+      uint8_t* dst = smem + kOffPool + stage * kStageBytes;
+      const int32_t prow = it.pool_base + i * kTilePools;
+      ptx::mbar_arrive_expect_tx(bar.full + stage, kStageBytes);
+      ptx::tma_load_2d_hint(dst, tmap_kp, bar.full + stage, 0, prow, pol_kp);
+      ptx::tma_load_2d_hint(dst + kPoolHalfBytes, tmap_kp, bar.full + stage, 64, prow, pol_kp);
+      ++fills;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+  }
+  if (!ok) {
+    record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+    *abort_flag = 1;
+  }
+  // drain: the last fill armed on each barrier must land before the CTA exits
+  for (uint32_t s = 0; s < kStages; ++s) {
+    const uint32_t armed = (fills + kStages - 1 - s) / kStages;  // fills that went to stage s
+    if (armed) ptx::mbar_wait_bounded(bar.full + s, (armed - 1) & 1, kMaxPolls, kMaxWaitNs);
+  }
+  if (q_armed) ptx::mbar_wait_bounded(bar.q_full, (q_armed - 1) & 1, kMaxPolls, kMaxWaitNs);
+}
+
+// MMA issuer (one thread of warp 1): for every pool tile of every item, 8 K16
+// tcgen05 MMAs of [128 pools x 128] x [128 x 256 query-head columns] into one of the
+// two TMEM accumulators, committed to the epilogue's acc_full barrier.
+__device__ __noinline__ void mma_role(const int32_t* cu, const int32_t* pool_off, const int2* items,
+                                      WorkspaceHeader* hdr, int kpool, uint32_t tmem_base) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Bars bar = bars_at(smem);
+  volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + kOffMisc + 4);
+  volatile int32_t* s_ring = reinterpret_cast<volatile int32_t*>(smem + kOffRing);
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTilePools, kN);
+  const uint32_t q_addr = ptx::smem_addr(smem + kOffQ);
+  const uint32_t pool_addr = ptx::smem_addr(smem + kOffPool);
+  int stage = 0, acc = 0;
+  uint32_t phase = 0, acc_phase = 0, q_phase = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int slot = r % kRing;
+    if (!ptx::mbar_wait_bounded(bar.ring_full + slot, uint32_t(r / kRing) & 1, kMaxPolls, kMaxWaitNs,
+                                kBackoffNs)) {
+      ok = false;
+      break;
+    }
+    const int idx = s_ring[slot];
+    ptx::mbar_arrive(bar.ring_empty + slot);
+    if (idx < 0) break;
+    const Item it = load_item(items, cu, pool_off, idx, kpool);
+    if (it.n_tiles == 0) continue;
+    if (!ptx::mbar_wait_bounded(bar.q_full, q_phase, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
+      ok = false;
+      break;
+    }
+    q_phase ^= 1;
+    ptx::tc_fence_after();
+    for (int i = 0; i < it.n_tiles; ++i) {
+      if (!ptx::mbar_wait_bounded(bar.acc_empty + acc, acc_phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) ||
+          !ptx::mbar_wait_bounded(bar.full + stage, phase, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
+      const uint32_t a_base = pool_addr + stage * kStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < kDim / 16; ++kk) {
+        const uint32_t a_addr = a_base + (kk >> 2) * kPoolHalfBytes + (kk & 3) * 32;
+        const uint32_t b_addr = q_addr + (kk >> 2) * kQHalfBytes + (kk & 3) * 32;
+        ptx::tc_mma_f16(d_tmem, ptx::smem_desc_kmajor_sw128(a_addr), ptx::smem_desc_kmajor_sw128(b_addr), idesc,
+                        kk > 0 ? 1u : 0u);
+      }
+      ptx::tc_commit(bar.empty + stage);
+      ptx::tc_commit(bar.acc_full + acc);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    if (!ok) break;
+    ptx::tc_commit(bar.q_empty);
+  }
+  if (!ok) {
+    record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+    *abort_flag = 1;
+  }
+  // every MMA issued above must complete before TMEM is released
+  ptx::tc_commit(bar.mma_done);
+  ptx::mbar_wait_bounded(bar.mma_done, 0, kMaxPolls, kMaxWaitNs);
+}
+
 template <bool kNegScale>
 __global__ void __launch_bounds__(kThreads, 1)
     select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
@@ -323,135 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int32_t* s_ring = reinterpret_cast<volatile int32_t*>(smem + kOffRing);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol_q = ptx::policy_evict_first();
-      const uint64_t pol_kp = ptx::policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0, q_phase = 0;
-      uint32_t fills = 0;  // pool-tile fills armed so far (stage = fill index mod kStages)
-      uint32_t q_armed = 0;
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
-        // next work item from the global counter (heaviest first, as the plan sorted
-        // them), handed to the MMA issuer and the epilogue through the ring
-        const int slot = r % kRing;
-        const uint32_t use = uint32_t(r / kRing);
-        if (use > 0 && !ptx::mbar_wait_bounded(bar.ring_empty + slot, (use - 1) & 1, kMaxPolls, kMaxWaitNs,
-                                               kBackoffNs)) {
-          ok = false;
-          break;
-        }
-        int idx = atomicAdd(&hdr->next_item, 1);
-        if (idx >= n_items) idx = -1;
-        s_ring[slot] = idx;
-        ptx::mbar_arrive(bar.ring_full + slot);
-        if (idx < 0) break;
-        const Item it = load_item(items, cu, pool_off, idx, kpool);
-        if (it.n_tiles == 0) continue;
-        if (!ptx::mbar_wait_bounded(bar.q_empty, q_phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
-          ok = false;
-          break;
-        }
-        q_phase ^= 1;
-        uint8_t* qdst = smem + kOffQ;
-        const int32_t qrow = int32_t((it.seq_start + it.t0) * kHeads);
-        ptx::mbar_arrive_expect_tx(bar.q_full, kQBytes);
-        ptx::tma_load_2d_hint(qdst, &tmap_q, bar.q_full, 0, qrow, pol_q);
-        ptx::tma_load_2d_hint(qdst + kQHalfBytes, &tmap_q, bar.q_full, 64, qrow, pol_q);
-        ++q_armed;
-        for (int i = 0; i < it.n_tiles; ++i) {
-          if (!ptx::mbar_wait_bounded(bar.empty + stage, phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) ||
-              *abort_flag) {
-            ok = false;
-            break;
-          }
-          uint8_t* dst = smem + kOffPool + stage * kStageBytes;
-          const int32_t prow = it.pool_base + i * kTilePools;
-          ptx::mbar_arrive_expect_tx(bar.full + stage, kStageBytes);
-          ptx::tma_load_2d_hint(dst, &tmap_kp, bar.full + stage, 0, prow, pol_kp);
-          ptx::tma_load_2d_hint(dst + kPoolHalfBytes, &tmap_kp, bar.full + stage, 64, prow, pol_kp);
-          ++fills;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-      if (!ok) {
-        record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
-        *abort_flag = 1;
-      }
-      // drain: the last fill armed on each barrier must land before the CTA exits
-      for (uint32_t s = 0; s < kStages; ++s) {
-        const uint32_t armed = (fills + kStages - 1 - s) / kStages;  // fills that went to stage s
-        if (armed) ptx::mbar_wait_bounded(bar.full + s, (armed - 1) & 1, kMaxPolls, kMaxWaitNs);
-      }
-      if (q_armed) ptx::mbar_wait_bounded(bar.q_full, (q_armed - 1) & 1, kMaxPolls, kMaxWaitNs);
-    }
+    if (lane == 0) producer_role(&tmap_q, &tmap_kp, cu, pool_off, items, hdr, kpool, n_items);
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTilePools, kN);
-      const uint32_t q_addr = ptx::smem_addr(smem + kOffQ);
-      const uint32_t pool_addr = ptx::smem_addr(smem + kOffPool);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0, q_phase = 0;
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int slot = r % kRing;
-        if (!ptx::mbar_wait_bounded(bar.ring_full + slot, uint32_t(r / kRing) & 1, kMaxPolls, kMaxWaitNs,
-                                    kBackoffNs)) {
-          ok = false;
-          break;
-        }
-        const int idx = s_ring[slot];
-        ptx::mbar_arrive(bar.ring_empty + slot);
-        if (idx < 0) break;
-        const Item it = load_item(items, cu, pool_off, idx, kpool);
-        if (it.n_tiles == 0) continue;
-        if (!ptx::mbar_wait_bounded(bar.q_full, q_phase, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
-          ok = false;
-          break;
-        }
-        q_phase ^= 1;
-        ptx::tc_fence_after();
-        for (int i = 0; i < it.n_tiles; ++i) {
-          if (!ptx::mbar_wait_bounded(bar.acc_empty + acc, acc_phase ^ 1, kMaxPolls, kMaxWaitNs, kBackoffNs) ||
-              !ptx::mbar_wait_bounded(bar.full + stage, phase, kMaxPolls, kMaxWaitNs, kBackoffNs) || *abort_flag) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t d_tmem = tmem_base + uint32_t(acc * kAccCols);
-          const uint32_t a_base = pool_addr + stage * kStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < kDim / 16; ++kk) {
-            const uint32_t a_addr = a_base + (kk >> 2) * kPoolHalfBytes + (kk & 3) * 32;
-            const uint32_t b_addr = q_addr + (kk >> 2) * kQHalfBytes + (kk & 3) * 32;
-            ptx::tc_mma_f16(d_tmem, ptx::smem_desc_kmajor_sw128(a_addr), ptx::smem_desc_kmajor_sw128(b_addr), idesc,
-                            kk > 0 ? 1u : 0u);
-          }
-          ptx::tc_commit(bar.empty + stage);
-          ptx::tc_commit(bar.acc_full + acc);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1;
-        }
-        if (!ok) break;
-        ptx::tc_commit(bar.q_empty);
-      }
-      if (!ok) {
-        record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
-        *abort_flag = 1;
-      }
-      // every MMA issued above must complete before TMEM is released
-      ptx::tc_commit(bar.mma_done);
-      ptx::mbar_wait_bounded(bar.mma_done, 0, kMaxPolls, kMaxWaitNs);
-    }
+    if (lane == 0) mma_role(cu, pool_off, items, hdr, kpool, tmem_base);
   } else {
     // ------------------------------------------------------------ epilogue
     // Row split: group grp (warps 2-5 -> 0, warps 6-9 -> 1) owns rows 4*grp .. 4*grp+3
