@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(kSelectThreads) rows_select_kernel(
     uint64_t k[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) k[h] = s_keys[64 * warp + 32 * h + lane];
-    block_sort512_desc(k, s_ties);  // k[h] is now rank 64 warp + 32 h + lane
+    block_sort512_desc(k, s_ties, 1);  // k[h] is now rank 64 warp + 32 h + lane
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int rank = 64 * warp + 32 * h + lane;

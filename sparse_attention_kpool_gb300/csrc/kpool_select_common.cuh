@@ -175,12 +175,17 @@ __device__ __forceinline__ void warp_sort512_blocked_desc(uint64_t (&k)[16]) {
   }
 }
 
-// Descending bitonic sort of 512 keys by a whole block of 256 threads: k[h] of
-// thread (warp w, lane l) is key 64 w + 32 h + l. Strides up to 16 go through
-// shuffles, stride 32 swaps the thread's two keys, strides 64..256 cross warps
-// through s_buf (1024 keys of shared memory, two alternating halves, so each such
-// stage needs one barrier). On return the thread holds ranks 64 w + 32 h + l.
-__device__ __forceinline__ void block_sort512_desc(uint64_t (&k)[2], uint64_t* s_buf) {
+__device__ __forceinline__ void group_bar(int id, int count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Descending bitonic sort of 512 keys by the 256 threads of warps 0-7 (named
+// barrier bar_id): k[h] of thread (warp w, lane l) is key 64 w + 32 h + l. Strides
+// up to 16 go through shuffles, stride 32 swaps the thread's two keys, strides
+// 64..256 cross warps through s_buf (1024 keys of shared memory, two alternating
+// halves, so each such stage needs one barrier). On return the thread holds ranks
+// 64 w + 32 h + l.
+__device__ __forceinline__ void block_sort512_desc(uint64_t (&k)[2], uint64_t* s_buf, int bar_id) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int half = 0;
 #pragma unroll
@@ -192,7 +197,7 @@ __device__ __forceinline__ void block_sort512_desc(uint64_t (&k)[2], uint64_t* s
         half ^= 1;
 #pragma unroll
         for (int h = 0; h < 2; ++h) b[64 * warp + 32 * h + lane] = k[h];
-        __syncthreads();
+        group_bar(bar_id, 256);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int i = 64 * warp + 32 * h + lane;
@@ -214,10 +219,6 @@ __device__ __forceinline__ void block_sort512_desc(uint64_t (&k)[2], uint64_t* s
       }
     }
   }
-}
-
-__device__ __forceinline__ void group_bar(int id, int count) {
-  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Scratch (shared memory) of block_select_compact: per-warp OR/AND words, three
