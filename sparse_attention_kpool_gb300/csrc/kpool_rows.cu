@@ -54,6 +54,15 @@ constexpr int kCollectThreads = 256;
 constexpr int kCollectPer = kCollectPools / kCollectThreads;  // R2: scores per thread and round
 static_assert(kCollectPer % 4 == 0, "R2 loads its scores 4 at a time");
 
+// Programmatic dependent launch: R1-R3 are launched so they may start while the
+// kernel before them is still running; each waits here, before its first read of
+// anything an earlier kernel of the call wrote, until that kernel has completed
+// and its writes are visible. (Launched without the attribute, the wait returns at
+// once.) The trigger lets the next kernel's CTAs be scheduled as early as the
+// resources they need free up.
+__device__ __forceinline__ void wait_prior_kernel() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_kernel() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 struct RowInfo {
   int32_t pool_base;  // global pooled-key row of the sequence's pool 0
   int32_t e;          // eligible pools floor((t+1)/kpool); -1 marks an invalid row
@@ -96,6 +105,7 @@ __global__ void __launch_bounds__(256) rows_plan_kernel(const int32_t* __restric
   __shared__ int s_bad, s_bad_row;
   __shared__ int s_warp[32];
   const int tid = threadIdx.x;
+  allow_next_kernel();
   if (tid == 0) {
     s_bad = (cu[0] != 0 || int64_t(cu[S]) != T) ? 1 : 0;
     s_bad_row = 0;
@@ -179,6 +189,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
     float scale, float* __restrict__ scores, int64_t stride, uint32_t* __restrict__ hist) {
   __shared__ uint32_t s_hist[kHistBins];  // this unit's histogram, flushed to the row's at the end
   __shared__ uint4 s_q[16][32];           // the row's query fragments (see below)
+  wait_prior_kernel();  // the plan: n_items, row records, unit offsets (and the cleared histograms)
+  allow_next_kernel();
   const int n_units = hdr->n_items;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -342,6 +354,8 @@ __global__ void __launch_bounds__(kCollectThreads) rows_collect_kernel(
   __shared__ uint64_t s_a[kRowsMaxBudget];
   __shared__ uint64_t s_t[kCollectTies];
   const int r = blockIdx.y;
+  wait_prior_kernel();  // R1's scores and histograms
+  allow_next_kernel();
   if (hdr->n_levels == 0) return;
   const RowInfo ri = info[r];
   const int e = ri.e;
@@ -432,6 +446,7 @@ __global__ void __launch_bounds__(kSelectThreads) rows_select_kernel(
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const int width = budget * kpool + kpool;
   int32_t* tok = out_tokens + int64_t(r) * width;
+  wait_prior_kernel();  // R2's gather lists and counts
   // the row record and both gather counts in one round of loads (without valid
   // cu_seqlens the record is never read)
   const int n_levels = hdr->n_levels;
@@ -601,6 +616,26 @@ __global__ void __launch_bounds__(kSelectThreads) rows_select_kernel(
 
 // ------------------------------------------------------------------ host side
 
+namespace {
+// Launches `kern` with programmatic stream serialization: it may begin while the
+// previous kernel on the stream runs and waits for it in wait_prior_kernel().
+// Captured into a graph, the dependency becomes a programmatic edge.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_prior(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+}  // namespace
+
 RowsLayout rows_layout(int32_t R, int64_t T, int32_t S, int32_t kpool) {
   RowsLayout L{};
   int64_t stride = T / kpool;
@@ -659,21 +694,23 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
   const int64_t max_units = int64_t(R) * ((L.stride + kUnitPools - 1) / kUnitPools);
   int grid = int(max_units < int64_t(2) * num_sms ? (max_units > 0 ? max_units : 1) : int64_t(2) * num_sms);
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
-  rows_score_kernel<<<grid, kScoreWarps * 32, 0, stream>>>(static_cast<const uint4*>(q), w,
-                                                             static_cast<const uint4*>(kp), info, unit_off, hdr,
-                                                             R, scale, scores, L.stride, hist);
-  e = cudaGetLastError();
+  e = launch_after_prior(rows_score_kernel, dim3(grid), dim3(kScoreWarps * 32), stream, static_cast<const uint4*>(q),
+                         w, static_cast<const uint4*>(kp), static_cast<const RowInfo*>(info),
+                         static_cast<const int32_t*>(unit_off), static_cast<const WorkspaceHeader*>(hdr), R, scale,
+                         scores, L.stride, hist);
   if (e == cudaSuccess) e = mark(2);
   if (e != cudaSuccess) return e;
   const int64_t slices = (L.stride + kCollectPools - 1) / kCollectPools;
   const dim3 cgrid(unsigned(slices < kCollectCtasPerRow ? slices : kCollectCtasPerRow), unsigned(R));
-  rows_collect_kernel<<<cgrid, kCollectThreads, 0, stream>>>(scores, L.stride, info, hdr, budget, hist, cand_cnt,
-                                                              cand, tie_cnt, ties);
-  e = cudaGetLastError();
+  e = launch_after_prior(rows_collect_kernel, cgrid, dim3(kCollectThreads), stream, static_cast<const float*>(scores),
+                         L.stride, static_cast<const RowInfo*>(info), static_cast<const WorkspaceHeader*>(hdr), budget,
+                         static_cast<const uint32_t*>(hist), cand_cnt, cand, tie_cnt, ties);
   if (e != cudaSuccess) return e;
-  rows_select_kernel<<<R, kSelectThreads, 0, stream>>>(scores, L.stride, info, hdr, kpool, budget, cand_cnt, cand,
-                                                       tie_cnt, ties, out_ids, out_scores, out_tokens);
-  e = cudaGetLastError();
+  e = launch_after_prior(rows_select_kernel, dim3(R), dim3(kSelectThreads), stream, static_cast<const float*>(scores),
+                         L.stride, static_cast<const RowInfo*>(info), static_cast<const WorkspaceHeader*>(hdr), kpool,
+                         budget, static_cast<const int32_t*>(cand_cnt), static_cast<const uint64_t*>(cand),
+                         static_cast<const int32_t*>(tie_cnt), static_cast<const uint64_t*>(ties), out_ids, out_scores,
+                         out_tokens);
   if (e == cudaSuccess) e = mark(3);
   return e;
 }
