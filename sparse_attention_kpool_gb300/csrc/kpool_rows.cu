@@ -22,7 +22,8 @@
 //   R3 rows_select_kernel (1 CTA / row) exact top-budget among the gathered pools
 //                                   (ties to the smaller pool; a full MSD radix
 //                                   search over the row when the bin overflows), a
-//                                   register bitonic sort, ids / scores / tokens
+//                                   256-thread bitonic sort, ids / scores / tokens
+// R1-R3 use programmatic dependent launch (see wait_prior_kernel below).
 // R1 streams the pooled keys once per row (HBM-bound: 256 B per pool); the
 // contraction per pool is 32 heads x 128 channels, small enough that the
 // warp-level mma.sync form keeps up with memory, so the tcgen05 pipeline of the
