@@ -46,6 +46,9 @@ from sparse_attention_kpool_gb300 import workloads as W  # noqa: E402
 METRIC = "KPool selection sec @512k tokens; scored pairs/s; % of bf16 tensor-core peak"
 UNIT = "scored pairs/s"
 FLOP_PER_PAIR_PER_HEAD_DIM = 2  # one multiply-add per (head, channel) of a scored pair
+# The pages' unsharded KPool selection microbenchmark at 512k tokens per sequence,
+# seconds per rank (NVIDIA/Megatron-LM pull request #8299, "Validation" table).
+PAGES_SEC_512K = 21.07
 
 # DRAM traffic of the score+select kernel from one ncu capture, per launch at the
 # pages-scale workload, tied to the kernel source it was measured on: when the
@@ -672,6 +675,13 @@ def main():
         "gpu_launches": 4 * args.steps,
         "e2e": e2e,
     }
+    if wl.name == "pages_512k":
+        # the pages' own figure, context only (vs_baseline stays null): a different
+        # implementation that scores the full query x pool rectangle, on another GPU
+        line["pages_context"] = {
+            "sec_per_selection": PAGES_SEC_512K, "hardware": "one B200 (as the pages state)",
+            "work": "full query x pool rectangle (2x the causal pairs counted here)",
+            "ratio_of_seconds": PAGES_SEC_512K / (ms_step / 1e3)}
 
     if rank == 0 and not args.no_cpu:
         rows = pick_sample_rows(wl, args.cpu_sample_pairs, seed=7)
