@@ -47,7 +47,7 @@ METRIC = "KPool selection sec @512k tokens; scored pairs/s; % of bf16 tensor-cor
 UNIT = "scored pairs/s"
 FLOP_PER_PAIR_PER_HEAD_DIM = 2  # one multiply-add per (head, channel) of a scored pair
 # The pages' unsharded KPool selection microbenchmark at 512k tokens per sequence,
-# seconds per rank (NVIDIA/Megatron-LM pull request #8299, "Validation" table).
+# seconds per rank (NVIDIA/Megatron-LM pull request #8299, "Validation (from SkyRL)").
 PAGES_SEC_512K = 21.07
 
 # DRAM traffic of the score+select kernel from one ncu capture, per launch at the
