@@ -192,3 +192,34 @@ def test_rows_any_score_grid_gives_the_same_result(max_ctas):
     np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
     np.testing.assert_array_equal(toks.cpu().numpy(), toks_ref)
     np.testing.assert_array_equal(sc.cpu().numpy(), sc_ref)
+
+
+def test_rows_graph_replay_equals_eager():
+    """The step captured into a CUDA graph (the score, collect and select kernels then
+    hang off programmatic edges) and replayed gives the eager result every time."""
+    wl = W.DECODE_SMALL
+    inp = W.generate_rows(wl, "cuda")
+    ids_ref, toks_ref, sc_ref, _ = _run_rows(wl, inp)
+    kp = K.kpool_pool_keys(inp["k"], inp["cu_seqlens"], wl.kpool)
+    ws = K.new_rows_workspace(wl.num_rows, wl.total_tokens, wl.num_seqs, wl.kpool, wl.index_topk)
+    ids = torch.empty((wl.num_rows, wl.budget), dtype=torch.int32, device="cuda")
+    toks = torch.empty((wl.num_rows, wl.width), dtype=torch.int32, device="cuda")
+    sc = torch.empty((wl.num_rows, wl.budget), dtype=torch.float32, device="cuda")
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gs):
+        with torch.cuda.graph(graph, stream=gs):
+            K.kpool_select_rows(inp["q"], inp["w"], inp["row_seq"], inp["row_pos"], kp, inp["cu_seqlens"],
+                                wl.total_tokens, wl.kpool, wl.index_topk, wl.scale, out_pool_ids=ids,
+                                out_token_ids=toks, out_pool_scores=sc, workspace=ws, stream=gs)
+    torch.cuda.current_stream().wait_stream(gs)
+    for _ in range(3):
+        ids.fill_(CANARY)
+        toks.fill_(CANARY)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert K.kpool_last_device_error(ws) == K.KPOOL_OK
+        np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+        np.testing.assert_array_equal(toks.cpu().numpy(), toks_ref)
+        np.testing.assert_array_equal(sc.cpu().numpy(), sc_ref)
