@@ -4,6 +4,8 @@ Bit-exact comparison for integer-valued inputs; for float inputs the rule is:
   * every GPU pool score is within TOL_REL * max(|s_ref|, 1e-3 * rowmax|s_ref|)
     of the oracle's fp64 score of the same (row, pool);
   * the number of chosen pools and the tail match exactly;
+  * the chosen pools are distinct and causally eligible, and the expanded token
+    slots follow the GPU's own pool ids exactly;
   * the chosen set equals the oracle's, except that every pool in the symmetric
     difference scores (per the oracle) within that tolerance of the row's
     cutoff score -- near-ties may go either way;
@@ -65,8 +67,17 @@ def compare_float(inp: dict, wl, ref: dict, gpu_ids: np.ndarray, gpu_scores: np.
         # tail slots are pure index arithmetic: exact
         np.testing.assert_array_equal(gpu_tokens[i, B * wl.kpool:], ref["token_ids"][i, B * wl.kpool:],
                                       err_msg=f"row {row}: tail")
+        # the expanded slots follow the GPU's own pool ids exactly
+        kpl = np.arange(wl.kpool, dtype=np.int64)
+        expect = np.where(gid[:, None] >= 0, gid[:, None].astype(np.int64) * wl.kpool + kpl, -1).ravel()
+        np.testing.assert_array_equal(gpu_tokens[i, :B * wl.kpool], expect, err_msg=f"row {row}: expanded slots")
         if m == 0:
             continue
+        # chosen pools are distinct and causally eligible for this row
+        b_row = int(np.searchsorted(cu, row, side="right") - 1)
+        e_row = (int(row) - int(cu[b_row]) + 1) // wl.kpool
+        assert len(set(gid[:m].tolist())) == m, f"row {row}: repeated pool ids"
+        assert int(gid[:m].max()) < e_row, f"row {row}: pool {int(gid[:m].max())} is not eligible (e = {e_row})"
         if np.array_equal(rid, gid):
             same = True
         else:
