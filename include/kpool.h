@@ -203,7 +203,10 @@ kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, in
  * R = 0 is a valid no-op. A row whose row_seq or row_pos is out of range gets
  * all -1 outputs and the call records KPOOL_ERR_INVALID_ARG on the device
  * (kpool_last_device_error); malformed cu_seqlens records the same and every
- * row gets -1 outputs.
+ * row gets -1 outputs. The call allocates and synchronises nothing, so a decode
+ * loop can capture it into a CUDA graph; its second to fourth kernels are
+ * launched with programmatic stream serialization (each waits on the device for
+ * the one before it).
  */
 size_t kpool_rows_workspace_bytes(int32_t num_rows, int64_t total_tokens, int32_t num_seqs, int32_t kpool,
                                   int32_t index_topk);
