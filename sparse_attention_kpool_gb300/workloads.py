@@ -145,21 +145,25 @@ def _plant_duplicate_pools(k: torch.Tensor, cu: torch.Tensor, kpool: int, every:
 
 def sample_rows(wl: Workload, count: int, seed: int = 12345) -> torch.Tensor:
     """A stratified sample of global rows: each sequence's first and last rows, rows at
-    every kpool phase near the ends, and uniform draws (sorted, unique, int64)."""
+    every kpool phase near the ends and around local row index_topk (where a row's
+    eligible pools first exceed the budget), and uniform draws (sorted, unique, int64)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     cu = wl.cu_seqlens().tolist()
     picks = set()
+    span = 2 * wl.kpool
     for b in range(wl.num_seqs):
         s, e = cu[b], cu[b + 1]
         if e <= s:
             continue
-        for t in list(range(s, min(e, s + 2 * wl.kpool + 1))) + list(range(max(s, e - 2 * wl.kpool), e)):
+        for t in list(range(s, min(e, s + span + 1))) + list(range(max(s, e - span), e)):
+            picks.add(t)
+        mid = s + wl.index_topk
+        for t in range(max(s, mid - span), min(e, mid + span + 1)):
             picks.add(t)
     T = wl.total_tokens
-    if T > 0:
-        need = max(0, count - len(picks))
-        picks.update(torch.randint(0, T, (need,), generator=g).tolist())
+    while len(picks) < min(count, T):  # uniform draws until `count` distinct rows
+        picks.update(torch.randint(0, T, (count - len(picks),), generator=g).tolist())
     return torch.tensor(sorted(picks), dtype=torch.int64)
 
 

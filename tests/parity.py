@@ -58,6 +58,8 @@ def compare_float(inp: dict, wl, ref: dict, gpu_ids: np.ndarray, gpu_scores: np.
     kp = ref["kp"]
     B = wl.budget
     near_tie_rows = 0
+    max_rel_err = 0.0    # largest |s_gpu - s_ref| / max(|s_ref|, 1e-3 rowmax) seen
+    scores_compared = 0
     q_cpu_cache = {}
     for i, row in enumerate(ref["rows"]):
         rid, gid = ref["pool_ids"][i], gpu_ids[i]
@@ -100,8 +102,11 @@ def compare_float(inp: dict, wl, ref: dict, gpu_ids: np.ndarray, gpu_scores: np.
         if gpu_scores is not None:
             for j in range(m):
                 sr = float(ref_scores[j]) if same else s_ref(int(gid[j]))
-                assert abs(float(gpu_scores[i, j]) - sr) <= _tol(ref_scores, sr), \
+                err = abs(float(gpu_scores[i, j]) - sr)
+                assert err <= _tol(ref_scores, sr), \
                     f"row {row} slot {j}: gpu score {gpu_scores[i, j]} vs oracle {sr}"
+                max_rel_err = max(max_rel_err, err / (_tol(ref_scores, sr) / TOL_REL))
+                scores_compared += 1
         if same:
             continue
         g_set, r_set = set(gid[:m].tolist()), set(rid[:m].tolist())
@@ -112,7 +117,18 @@ def compare_float(inp: dict, wl, ref: dict, gpu_ids: np.ndarray, gpu_scores: np.
         for j in range(m - 1):
             assert g_sc[j] >= g_sc[j + 1] - _tol(ref_scores, g_sc[j]), f"row {row}: order at slot {j}"
         near_tie_rows += 1
-    return {"rows": len(ref["rows"]), "near_tie_rows": near_tie_rows}
+    return {"rows": len(ref["rows"]), "near_tie_rows": near_tie_rows, "max_rel_err": max_rel_err,
+            "scores_compared": scores_compared}
+
+
+def cutoff_tie_rows(ref_wide: dict, budget: int) -> np.ndarray:
+    """Rows (indices into ref_wide) where an exact tie straddles the budget cutoff: the
+    budget-th and (budget+1)-th ranked scores are equal, so the tiebreak alone decides
+    which pool is kept. ref_wide is an oracle selection with at least budget + 1 slots."""
+    sc = ref_wide["scores"]
+    assert sc.shape[1] > budget
+    both = (ref_wide["pool_ids"][:, budget - 1] >= 0) & (ref_wide["pool_ids"][:, budget] >= 0)
+    return np.nonzero(both & (sc[:, budget - 1] == sc[:, budget]))[0]
 
 
 def assert_exact(ref: dict, gpu_ids: np.ndarray, gpu_tokens: np.ndarray):

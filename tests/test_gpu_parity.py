@@ -148,9 +148,21 @@ def test_tie_heavy_workload_exact():
     ref = full_oracle(inp, wl)
     parity.assert_exact(ref, ids, toks)
     check_properties(dev, wl, ids, sc, toks)
-    # the recipe does produce exact ties at the cutoff
-    kp = ref["kp"]
-    assert (ref["eligible"] > wl.budget).any()
+    # The bit-exact match above covers the tiebreak at the cutoff only if the workload
+    # has rows where an exact tie straddles it: rank budget and rank budget + 1 of the
+    # oracle's full ranking score the same, so only "smaller pool index first" decides
+    # which pool is kept. Count them with a one-slot-wider oracle selection.
+    wide = oracle.select(parity.bits(inp["q"]), inp["w"].numpy(), ref["kp"], inp["cu_seqlens"].numpy(),
+                         np.arange(wl.total_tokens), wl.dtype, wl.kpool, wl.index_topk + wl.kpool, wl.scale)
+    np.testing.assert_array_equal(wide["pool_ids"][:, :wl.budget], ref["pool_ids"])
+    tie_rows = parity.cutoff_tie_rows(wide, wl.budget)
+    print(f"tie_heavy: {len(tie_rows)} of {wl.total_tokens} rows have an exact tie straddling the "
+          f"budget-{wl.budget} cutoff")
+    assert len(tie_rows) > 0
+    # on those rows the kept pool at the cutoff is the smaller index of the tied pair
+    kept, dropped = wide["pool_ids"][tie_rows, wl.budget - 1], wide["pool_ids"][tie_rows, wl.budget]
+    assert (kept < dropped).all()
+    np.testing.assert_array_equal(ids[tie_rows, wl.budget - 1], kept)
 
 
 @pytest.mark.parametrize("kernel", [TC, SIMT])
@@ -229,7 +241,7 @@ def test_tiny_workload_f32():
     dev = to_dev(inp)
     ids, toks, sc = run(dev, wl)
     ref = full_oracle(inp, wl)
-    parity.compare_float(inp, wl, ref, ids, sc, toks)
+    report("tiny", parity.compare_float(inp, wl, ref, ids, sc, toks))
     check_properties(dev, wl, ids, sc, toks)
 
 
@@ -241,7 +253,24 @@ def test_float_small_all_rows():
     ref = full_oracle(inp, wl)
     stats = parity.compare_float(inp, wl, ref, ids, sc, toks)
     check_properties(dev, wl, ids, sc, toks)
+    report("float_small", stats)
     assert stats["near_tie_rows"] <= 0.05 * wl.total_tokens
+
+
+# Largest relative score error observed GPU vs oracle, as a share of the stated 1e-3
+# tolerance's denominator max(|s_ref|, 1e-3 rowmax). The tolerance is the acceptance
+# rule; this tighter bound catches a systematic error well inside it (a scale or weight
+# rounded to bf16, say, is ~4e-3 relative). fp32 accumulation of bf16 products over
+# d = 128 channels and 32 heads gives errors below 1e-6 (measured on a GB300: 2.8e-7 to
+# 5.2e-7 on every float workload).
+MAX_OBSERVED_REL_ERR = 1e-5
+
+
+def report(name, stats):
+    print(f"{name}: {stats['rows']} rows, {stats['scores_compared']} scores compared, max relative score error "
+          f"{stats['max_rel_err']:.3e}, rows differing from the oracle within the tie band "
+          f"{stats['near_tie_rows']} ({100.0 * stats['near_tie_rows'] / max(1, stats['rows']):.2f} %)")
+    assert stats["max_rel_err"] <= MAX_OBSERVED_REL_ERR
 
 
 def _sampled(wl, count):
@@ -254,6 +283,7 @@ def _sampled(wl, count):
     ref = parity.oracle_rows(dev, wl, rows)
     r = torch.as_tensor(rows, device="cuda")
     stats = parity.compare_float(dev, wl, ref, ids[r].cpu().numpy(), sc[r].cpu().numpy(), toks[r].cpu().numpy())
+    report(wl.name, stats)
     return stats
 
 
@@ -271,7 +301,8 @@ def test_long_128k_workload_sampled():
 
 
 def test_pages_512k_workload_sampled():
-    stats = _sampled(W.PAGES_512K, 96)
+    stats = _sampled(W.PAGES_512K, 1024)
+    assert stats["rows"] >= 1024
     assert stats["near_tie_rows"] <= 0.25 * stats["rows"]
 
 

@@ -458,3 +458,28 @@ def test_gated_pool_shift_invariance(lib=None):
     a = oracle.pool_gated(k, gate, ape, "bf16", cu, kpool, lib=lib)
     b = oracle.pool_gated(k, gate + np.float32(3.0), ape, "bf16", cu, kpool, lib=lib)
     np.testing.assert_array_equal(a, b)
+
+
+def test_tie_heavy_full_budget_has_cutoff_ties():
+    """At its full size and budget (2 x 4096 tokens, budget 512) the tie-heavy workload has
+    rows where an exact tie straddles the cutoff, so its bit-exact GPU comparison exercises
+    the smaller-index tiebreak at budget 512. Checked on a few of those rows by brute force."""
+    from tests import parity
+    wl = W.TIE_HEAVY
+    inp = W.generate(wl, "cpu")
+    cu = inp["cu_seqlens"].numpy()
+    kp = oracle.pool(bits(inp["k"]), wl.dtype, cu, wl.kpool)
+    q, w = values(inp["q"]), inp["w"].numpy()
+    wide = oracle.select(bits(inp["q"]), w, kp, cu, np.arange(wl.total_tokens), wl.dtype, wl.kpool,
+                         wl.index_topk + wl.kpool, wl.scale)
+    rows = parity.cutoff_tie_rows(wide, wl.budget)
+    assert len(rows) > 0
+    for i in rows[:: max(1, len(rows) // 5)][:5]:
+        t = int(i)
+        b = int(np.searchsorted(cu, t, side="right") - 1)
+        e = (t - int(cu[b]) + 1) // wl.kpool
+        pool0 = int(oracle.pool_offsets(cu, wl.kpool)[b])
+        s = brute_scores(q[t:t + 1], w[t:t + 1], kp[pool0:pool0 + e], wl.scale)[0]
+        order = np.lexsort((np.arange(e), -s))  # score descending, then pool ascending
+        np.testing.assert_array_equal(order[:wl.budget + 1], wide["pool_ids"][i])
+        assert s[order[wl.budget - 1]] == s[order[wl.budget]]

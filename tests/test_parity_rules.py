@@ -129,3 +129,79 @@ def test_exact_rule_rejects_any_change(case):
     ids[i, [0, 1]] = ids[i, [1, 0]]
     with pytest.raises(AssertionError):
         parity.assert_exact(ref, ids, tok)
+
+
+# ---------------------------------------------------- a packed batch of two sequences
+#
+# The rule works in sequence-local indices: the eligibility bound comes from the row's
+# own sequence in cu_seqlens, the oracle's pools are offset by that sequence's first
+# pool, and the expanded tokens count from the sequence's first token. Mistakes planted
+# in the second sequence (nonzero offsets) must be caught as well.
+
+@pytest.fixture(scope="module")
+def packed_case():
+    wl = W.custom("packed2", (41, 58), heads=4, head_dim=32, kpool=4, index_topk=16, scale=0.17,
+                  dtype="f32", values="normal", seed=9)
+    inp = W.generate(wl, "cpu")
+    rows = np.arange(wl.total_tokens, dtype=np.int64)
+    ref = parity.oracle_rows(inp, wl, rows)
+    return wl, inp, ref
+
+
+def _second_seq_full_row(wl, inp, ref):
+    cu = inp["cu_seqlens"].numpy()
+    for i in range(len(ref["rows"]) - 1, -1, -1):
+        if int(ref["rows"][i]) >= cu[1] and (ref["pool_ids"][i] >= 0).sum() == wl.budget:
+            return i, int(ref["rows"][i]) - int(cu[1])
+    raise AssertionError("no full row in the second sequence")
+
+
+def test_packed_oracle_answer_passes(packed_case):
+    wl, inp, ref = packed_case
+    ids, sc, tok = _copy(ref)
+    assert parity.compare_float(inp, wl, ref, ids, sc, tok)["near_tie_rows"] == 0
+
+
+def test_packed_rejects_batch_global_pool_ids(packed_case):
+    wl, inp, ref = packed_case
+    first_pool = int(inp["cu_seqlens"][1]) // wl.kpool  # pools of the first sequence
+    ids, sc, tok = _copy(ref)
+    i, _ = _second_seq_full_row(wl, inp, ref)
+    ids[i] = ids[i] + first_pool
+    tok[i, :wl.budget * wl.kpool] = (ids[i][:, None] * wl.kpool + np.arange(wl.kpool)).ravel()
+    with pytest.raises(AssertionError):
+        parity.compare_float(inp, wl, ref, ids, sc, tok)
+
+
+def test_packed_rejects_batch_global_token_ids(packed_case):
+    wl, inp, ref = packed_case
+    ids, sc, tok = _copy(ref)
+    i, _ = _second_seq_full_row(wl, inp, ref)
+    first_token = int(inp["cu_seqlens"][1])
+    tok[i, :wl.budget * wl.kpool] += first_token
+    with pytest.raises(AssertionError):
+        parity.compare_float(inp, wl, ref, ids, sc, tok)
+
+
+def test_packed_rejects_a_pool_just_past_the_rows_bound(packed_case):
+    wl, inp, ref = packed_case
+    ids, sc, tok = _copy(ref)
+    i, t = _second_seq_full_row(wl, inp, ref)
+    e = (t + 1) // wl.kpool  # sequence-local eligible pools of that row
+    ids[i, wl.budget - 1] = e
+    tok[i, (wl.budget - 1) * wl.kpool:wl.budget * wl.kpool] = e * wl.kpool + np.arange(wl.kpool)
+    with pytest.raises(AssertionError):
+        parity.compare_float(inp, wl, ref, ids, sc, tok)
+
+
+def test_packed_rejects_scores_of_the_wrong_sequence(packed_case):
+    """A kernel that scored the second sequence's row against the first sequence's pools."""
+    from oracle import oracle
+    wl, inp, ref = packed_case
+    ids, sc, tok = _copy(ref)
+    i, t = _second_seq_full_row(wl, inp, ref)
+    row = int(ref["rows"][i])
+    qr, wr = parity.bits(inp["q"][row]), inp["w"][row].numpy()
+    sc[i, :wl.budget] = [oracle.score(qr, wr, ref["kp"][int(p)], wl.dtype, wl.scale) for p in ids[i]]
+    with pytest.raises(AssertionError):
+        parity.compare_float(inp, wl, ref, ids, sc, tok)
