@@ -91,8 +91,29 @@ typedef struct {
                                  caller can time each kernel without a profiler; inside a
                                  stream capture they become event-record nodes of the
                                  graph, recorded again on every replay */
-  int32_t reserved[4];        /* must be zero */
+  int32_t row_begin;          /* with KPOOL_OPT_ROW_RANGE in flags: the call selects for the */
+  int32_t row_end;            /* global rows [row_begin, row_end) only (else both zero)    */
+  int32_t flags;              /* 0 or KPOOL_OPT_ROW_RANGE                                   */
+  int32_t reserved;           /* must be zero */
 } kpool_options;
+
+/*
+ * Query-row sharding ("NVIDIA/Megatron-LM pull request #8299", section "Change";
+ * "NovaSky-AI/SkyRL pull request #2422", Summary): rows are independent, so a
+ * group of G processes can each select a contiguous range of query rows and
+ * all-gather the int32 pool ids; expansion then runs on the gathered
+ * [T, budget] tensor (kpool_expand). With KPOOL_OPT_ROW_RANGE, kpool_select_ex
+ * and kpool_select_pooled take the whole batch's q, k (or pooled keys), w and
+ * cu_seqlens but score, select and expand only the global rows
+ * [row_begin, row_end), 0 <= row_begin <= row_end <= T. Their outputs then hold
+ * R = row_end - row_begin rows: out_pool_ids [R, budget], out_token_ids
+ * [R, index_topk + kpool], row i being global row row_begin + i, each exactly
+ * as the whole-batch call would write that row. An empty range is a no-op.
+ * As on the pages, the sharded path returns no index scores: out_pool_scores
+ * must be NULL (else KPOOL_ERR_INVALID_ARG). The workspace size is the
+ * whole batch's. kpool_balanced_row_split() gives ranges of equal work.
+ */
+#define KPOOL_OPT_ROW_RANGE 1
 
 /*
  * Workspace size, in bytes, for a call with these sizes. Pure host arithmetic;
@@ -124,6 +145,24 @@ kpool_status kpool_select_ex(const void* q, const void* k, const float* w, const
                              int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores,
                              void* workspace, size_t workspace_bytes, void* stream,
                              const kpool_options* options);
+
+/*
+ * Splits the rows of a packed batch into `parts` contiguous ranges of near-equal
+ * work for query-row sharding. cu_seqlens is a HOST array [num_seqs + 1] (as the
+ * device one); out_bounds, a HOST array of parts + 1 int32, receives
+ * 0 = b[0] <= b[1] <= ... <= b[parts] = T, range g being rows [b[g], b[g+1]).
+ * A row's work is its causal pair count floor((t+1)/kpool) (t sequence-local)
+ * plus row_weight (the per-row cost of ranking, in pair units; 0 balances pairs
+ * alone). The split minimises nothing globally: boundary g is the first row at
+ * which the running work reaches g/parts of the total, so every range's work is
+ * within one row's work of an equal share. The pages split rows evenly
+ * (rank r takes rows [r*ceil(sq/G), ...)); under the causal mask that gives the
+ * last rank about 2G-1 times the first rank's pairs, which this split avoids.
+ * Pure host code; returns KPOOL_ERR_INVALID_ARG for malformed cu_seqlens,
+ * kpool < 1, parts < 1 or row_weight < 0.
+ */
+kpool_status kpool_balanced_row_split(const int32_t* cu_seqlens, int32_t num_seqs, int32_t kpool,
+                                      int64_t row_weight, int32_t parts, int32_t* out_bounds);
 
 /*
  * Step 1 alone: writes the pooled keys [P, d] (dtype, P = sum_b floor(L_b/kpool),
@@ -265,23 +304,36 @@ kpool_status kpool_wait_timeout_selftest(void* workspace, size_t workspace_bytes
  * the scratch taken from a file-scope __device__ array of
  * KPOOL_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the
  * process exits. Inputs and outputs are still the caller's device buffers.
- *   - A call whose kpool_workspace_bytes(...) exceeds KPOOL_STATIC_SCRATCH_BYTES
- *     returns KPOOL_ERR_WORKSPACE before any GPU work.
+ *   - The arguments are checked as kpool_select checks them, so a shape the
+ *     kernels do not implement returns KPOOL_ERR_UNSUPPORTED at any size. Only a
+ *     call that passes those checks and whose kpool_workspace_bytes(...) exceeds
+ *     KPOOL_STATIC_SCRATCH_BYTES returns KPOOL_ERR_WORKSPACE (split the batch),
+ *     before any GPU work.
  *   - The first call on each device looks up the array's device address (with
  *     that device current) and caches it: make that first call before any
  *     stream capture.
  *   - All calls on a device share the one array, which keeps the last call's
  *     contents: calls that overlap on the GPU race and must be serialised.
  *   - It allocates nothing (no cudaMalloc/cudaFree or allocating library call).
- *   - Device-side errors land in the shared array's header, which the caller
- *     cannot name, so they are not reported (malformed cu_seqlens leaves the
- *     outputs unwritten, as with kpool_select).
+ *   - Errors found on the device (malformed cu_seqlens, which leaves the outputs
+ *     unwritten as with kpool_select; a bounded wait that ran out) land in the
+ *     shared array's header: read them with
+ *     kpool_static_scratch_last_device_error().
  */
 kpool_status kpool_select_static_scratch(const void* q, const void* k, const float* w,
                                          const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                                          int32_t heads, int32_t head_dim, kpool_dtype dtype, int32_t kpool,
                                          int32_t index_topk, float scale, int32_t* out_pool_ids,
                                          int32_t* out_token_ids, float* out_pool_scores, void* stream);
+
+/*
+ * kpool_last_device_error for kpool_select_static_scratch: synchronises `stream`,
+ * then returns the device error word the last call on this device's built-in
+ * scratch array recorded (KPOOL_OK, KPOOL_ERR_INVALID_ARG for malformed
+ * cu_seqlens, KPOOL_ERR_DEVICE_TIMEOUT, KPOOL_ERR_INTERNAL), or KPOOL_ERR_CUDA if
+ * the look-up, synchronisation or copy failed. Allocates nothing.
+ */
+kpool_status kpool_static_scratch_last_device_error(void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* kpool_status_string(kpool_status status);

@@ -90,6 +90,64 @@ size_t kpool_workspace_bytes(int64_t total_tokens, int32_t num_seqs, int32_t hea
 
 }  // extern "C"
 
+namespace kpool {
+
+kpool_status select_check_args(const void* q, const void* kin, const float* w, const int32_t* cu_seqlens,
+                               int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                               kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                               const int32_t* out_pool_ids, const int32_t* out_token_ids,
+                               const float* out_pool_scores, const kpool_options* options, bool* use_tc,
+                               int64_t* row_begin, int64_t* row_end) {
+  kpool_options opt{};
+  if (options) opt = *options;
+  if (opt.reserved != 0 || (opt.flags & ~KPOOL_OPT_ROW_RANGE) != 0) return KPOOL_ERR_INVALID_ARG;
+  if (opt.score_kernel < KPOOL_SCORE_AUTO || opt.score_kernel > KPOOL_SCORE_SIMT || opt.max_ctas < 0)
+    return KPOOL_ERR_INVALID_ARG;
+
+  kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
+  if (st != KPOOL_OK) return st;
+  if (heads < 1 || index_topk < 0 || index_topk % kpool != 0 || !isfinite(scale)) return KPOOL_ERR_INVALID_ARG;
+  *row_begin = 0;
+  *row_end = total_tokens;
+  if (opt.flags & KPOOL_OPT_ROW_RANGE) {
+    // a shard of query rows; as on the pages, the sharded path returns no index scores
+    if (opt.row_begin < 0 || opt.row_begin > opt.row_end || int64_t(opt.row_end) > total_tokens ||
+        out_pool_scores != nullptr)
+      return KPOOL_ERR_INVALID_ARG;
+    *row_begin = opt.row_begin;
+    *row_end = opt.row_end;
+  } else if (opt.row_begin != 0 || opt.row_end != 0) {
+    return KPOOL_ERR_INVALID_ARG;
+  }
+  const int32_t budget = index_topk / kpool;
+  *use_tc = false;
+  if (total_tokens == 0 || *row_end == *row_begin) return KPOOL_OK;
+  if (!q || !kin || !w || !cu_seqlens || !out_token_ids || (budget > 0 && !out_pool_ids))
+    return KPOOL_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kin, 16) || !aligned(w, 4) || !aligned(cu_seqlens, 4) ||
+      !aligned(out_pool_ids, 4) || !aligned(out_token_ids, 4) || !aligned(out_pool_scores, 4))
+    return KPOOL_ERR_INVALID_ARG;
+
+  const bool tc_ok = select_tc_supported(dtype, heads, head_dim, budget);
+  const bool simt_ok = heads <= 64 && head_dim <= 256 && budget <= 4096;
+  switch (opt.score_kernel) {
+    case KPOOL_SCORE_TC:
+      if (!tc_ok) return KPOOL_ERR_UNSUPPORTED;
+      *use_tc = true;
+      break;
+    case KPOOL_SCORE_SIMT:
+      if (!simt_ok) return KPOOL_ERR_UNSUPPORTED;
+      *use_tc = false;
+      break;
+    default:
+      if (!tc_ok && !simt_ok) return KPOOL_ERR_UNSUPPORTED;
+      *use_tc = tc_ok;
+  }
+  return KPOOL_OK;
+}
+
+}  // namespace kpool
+
 namespace {
 
 // The whole selection; pools k itself when `pooled_in` is null, else scores the
@@ -99,42 +157,18 @@ kpool_status select_impl(const void* q, const void* k, const void* pooled_in, co
                          int32_t head_dim, kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
                          int32_t* out_pool_ids, int32_t* out_token_ids, float* out_pool_scores, void* workspace,
                          size_t workspace_bytes, void* stream_ptr, const kpool_options* options) {
+  const void* kin = pooled_in ? pooled_in : k;
+  bool use_tc = false;
+  int64_t rb = 0, re = 0;
+  kpool_status st = select_check_args(q, kin, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool,
+                                      index_topk, scale, out_pool_ids, out_token_ids, out_pool_scores, options,
+                                      &use_tc, &rb, &re);
+  if (st != KPOOL_OK) return st;
+  const int64_t T = total_tokens;
+  if (T == 0 || re == rb) return KPOOL_OK;
   kpool_options opt{};
   if (options) opt = *options;
-  for (int i = 0; i < 4; ++i)
-    if (opt.reserved[i] != 0) return KPOOL_ERR_INVALID_ARG;
-  if (opt.score_kernel < KPOOL_SCORE_AUTO || opt.score_kernel > KPOOL_SCORE_SIMT || opt.max_ctas < 0)
-    return KPOOL_ERR_INVALID_ARG;
-
-  kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
-  if (st != KPOOL_OK) return st;
-  if (heads < 1 || index_topk < 0 || index_topk % kpool != 0 || !isfinite(scale)) return KPOOL_ERR_INVALID_ARG;
   const int32_t budget = index_topk / kpool;
-  const int64_t T = total_tokens;
-  if (T == 0) return KPOOL_OK;
-  const void* kin = pooled_in ? pooled_in : k;
-  if (!q || !kin || !w || !cu_seqlens || !out_token_ids || (budget > 0 && !out_pool_ids))
-    return KPOOL_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(kin, 16) || !aligned(w, 4) || !aligned(cu_seqlens, 4) ||
-      !aligned(out_pool_ids, 4) || !aligned(out_token_ids, 4) || !aligned(out_pool_scores, 4))
-    return KPOOL_ERR_INVALID_ARG;
-
-  const bool tc_ok = select_tc_supported(dtype, heads, head_dim, budget);
-  const bool simt_ok = heads <= 64 && head_dim <= 256 && budget <= 4096;
-  bool use_tc;
-  switch (opt.score_kernel) {
-    case KPOOL_SCORE_TC:
-      if (!tc_ok) return KPOOL_ERR_UNSUPPORTED;
-      use_tc = true;
-      break;
-    case KPOOL_SCORE_SIMT:
-      if (!simt_ok) return KPOOL_ERR_UNSUPPORTED;
-      use_tc = false;
-      break;
-    default:
-      if (!tc_ok && !simt_ok) return KPOOL_ERR_UNSUPPORTED;
-      use_tc = tc_ok;
-  }
 
   const WorkspaceLayout L = workspace_layout(T, num_seqs, head_dim, elem_bytes(dtype), kpool);
   st = check_workspace(workspace, workspace_bytes, L);
@@ -151,7 +185,7 @@ kpool_status select_impl(const void* q, const void* k, const void* pooled_in, co
     return ev == nullptr || cuda_ok(record_stage_event(ev[i], stream));
   };
   if (!mark(0)) return KPOOL_ERR_CUDA;
-  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, T, kpool, ws, L, stream)) || !mark(1)) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, T, kpool, rb, re, ws, L, stream)) || !mark(1)) return KPOOL_ERR_CUDA;
   if (!pooled_in &&
       !cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, ws + L.pooled, ws, L, sms, stream)))
     return KPOOL_ERR_CUDA;
@@ -161,16 +195,17 @@ kpool_status select_impl(const void* q, const void* k, const void* pooled_in, co
     if (use_tc) {
       int grid = sms;
       if (opt.max_ctas > 0 && opt.max_ctas < grid) grid = opt.max_ctas;
-      e = launch_select_tc(q, pooled, w, cu_seqlens, num_seqs, T, kpool, budget, scale, out_pool_ids,
+      e = launch_select_tc(q, pooled, w, cu_seqlens, num_seqs, T, kpool, budget, scale, rb, re, out_pool_ids,
                            out_pool_scores, ws, L, grid, stream);
     } else {
-      e = launch_select_simt(q, pooled, w, dtype, cu_seqlens, num_seqs, T, heads, head_dim, kpool, budget, scale,
-                             out_pool_ids, out_pool_scores, ws, L, opt.max_ctas > 0 ? opt.max_ctas : sms, stream);
+      e = launch_select_simt(q, pooled, w, dtype, cu_seqlens, num_seqs, T, heads, head_dim, kpool, budget, scale, rb,
+                             re, out_pool_ids, out_pool_scores, ws, L, opt.max_ctas > 0 ? opt.max_ctas : sms,
+                             stream);
     }
     if (!cuda_ok(e)) return KPOOL_ERR_CUDA;
   }
   if (!mark(3)) return KPOOL_ERR_CUDA;
-  if (!cuda_ok(launch_expand(out_pool_ids, cu_seqlens, num_seqs, T, kpool, budget, out_token_ids,
+  if (!cuda_ok(launch_expand(out_pool_ids, cu_seqlens, num_seqs, rb, re, kpool, budget, out_token_ids,
                              reinterpret_cast<const WorkspaceHeader*>(ws + L.header), sms, stream)) ||
       !mark(4))
     return KPOOL_ERR_CUDA;
@@ -228,7 +263,8 @@ kpool_status kpool_pool_keys(const void* k, const int32_t* cu_seqlens, int32_t n
   int sms = 0;
   if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, ws, L, stream))) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, 0, total_tokens, ws, L, stream)))
+    return KPOOL_ERR_CUDA;
   if (!cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool, out_pooled_keys, ws, L,
                            sms, stream)))
     return KPOOL_ERR_CUDA;
@@ -254,7 +290,8 @@ kpool_status kpool_pool_keys_gated(const void* k, const float* gate, const float
   int sms = 0;
   if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, ws, L, stream))) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, 0, total_tokens, ws, L, stream)))
+    return KPOOL_ERR_CUDA;
   if (!cuda_ok(launch_pool_gated(k, gate, ape, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool,
                                  out_pooled_keys, ws, L, sms, stream)))
     return KPOOL_ERR_CUDA;
@@ -273,7 +310,7 @@ kpool_status kpool_expand(const int32_t* pool_ids, const int32_t* cu_seqlens, in
   if (!aligned(pool_ids, 4) || !aligned(out_token_ids, 4) || !aligned(cu_seqlens, 4)) return KPOOL_ERR_INVALID_ARG;
   int sms = 0;
   if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
-  if (!cuda_ok(launch_expand(pool_ids, cu_seqlens, num_seqs, total_tokens, kpool, budget, out_token_ids, nullptr,
+  if (!cuda_ok(launch_expand(pool_ids, cu_seqlens, num_seqs, 0, total_tokens, kpool, budget, out_token_ids, nullptr,
                              sms, static_cast<cudaStream_t>(stream_ptr))))
     return KPOOL_ERR_CUDA;
   return KPOOL_OK;
@@ -308,8 +345,7 @@ kpool_status kpool_select_rows_ex(const void* q, const float* w, const int32_t* 
                                   const kpool_options* options) {
   kpool_options opt{};
   if (options) opt = *options;
-  for (int i = 0; i < 4; ++i)
-    if (opt.reserved[i] != 0) return KPOOL_ERR_INVALID_ARG;
+  if (opt.reserved != 0 || opt.flags != 0 || opt.row_begin != 0 || opt.row_end != 0) return KPOOL_ERR_INVALID_ARG;
   if (opt.score_kernel != KPOOL_SCORE_AUTO || opt.max_ctas < 0) return KPOOL_ERR_INVALID_ARG;
   kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
   if (st != KPOOL_OK) return st;
@@ -356,6 +392,45 @@ kpool_status kpool_wait_timeout_selftest(void* workspace, size_t workspace_bytes
   if (!cuda_ok(launch_wait_selftest(static_cast<char*>(workspace), spin_limit,
                                     static_cast<cudaStream_t>(stream_ptr))))
     return KPOOL_ERR_CUDA;
+  return KPOOL_OK;
+}
+
+kpool_status kpool_balanced_row_split(const int32_t* cu_seqlens, int32_t num_seqs, int32_t kpool, int64_t row_weight,
+                                      int32_t parts, int32_t* out_bounds) {
+  if (cu_seqlens == nullptr || out_bounds == nullptr || num_seqs < 0 || kpool < 1 || parts < 1 || row_weight < 0)
+    return KPOOL_ERR_INVALID_ARG;
+  if (cu_seqlens[0] != 0) return KPOOL_ERR_INVALID_ARG;
+  for (int32_t b = 0; b < num_seqs; ++b)
+    if (cu_seqlens[b + 1] < cu_seqlens[b]) return KPOOL_ERR_INVALID_ARG;
+  const int64_t T = cu_seqlens[num_seqs];
+  // pairs of the first m rows of a sequence: sum_{i=1..m} floor(i / kpool)
+  auto pairs_prefix = [kpool](int64_t m) {
+    const int64_t n = m / kpool, r = m % kpool;
+    return int64_t(kpool) * n * (n - 1) / 2 + n * (r + 1);
+  };
+  auto work = [&](int64_t m) { return pairs_prefix(m) + m * row_weight; };  // first m rows of a sequence
+  int64_t total = 0;
+  for (int32_t b = 0; b < num_seqs; ++b) total += work(cu_seqlens[b + 1] - cu_seqlens[b]);
+  // boundary g is the first row r whose preceding rows' work reaches g * total / parts
+  const int64_t quot = total / parts, rem = total % parts;
+  auto target = [&](int64_t g) { return quot * g + (rem * g) / parts; };
+  out_bounds[0] = 0;
+  int32_t g = 1;
+  int64_t before = 0;  // work of the sequences before b
+  for (int32_t b = 0; b < num_seqs && g < parts; ++b) {
+    const int64_t len = cu_seqlens[b + 1] - cu_seqlens[b];
+    const int64_t wb = work(len);
+    while (g < parts && target(g) <= before + wb) {
+      int64_t lo = 0, hi = len;  // smallest m in [0, len] with before + work(m) >= target(g)
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) / 2;
+        if (before + work(mid) >= target(g)) hi = mid; else lo = mid + 1;
+      }
+      out_bounds[g++] = int32_t(cu_seqlens[b] + lo);
+    }
+    before += wb;
+  }
+  for (; g <= parts; ++g) out_bounds[g] = int32_t(T);
   return KPOOL_OK;
 }
 

@@ -49,19 +49,20 @@ __device__ __forceinline__ int32_t token_at(const RowInfo& ri, int32_t pool, int
 // row's 16-byte chunks l, l + 32, ...; chunk j < budget expands pool rank j, chunk
 // budget holds the tail. 32-bit arithmetic throughout.
 __global__ void __launch_bounds__(256) expand_kernel_k4(const int32_t* __restrict__ pool_ids,
-                                                        const int32_t* __restrict__ cu, int S, int64_t T,
-                                                        int budget, int32_t* __restrict__ out,
+                                                        const int32_t* __restrict__ cu, int S, int64_t row_begin,
+                                                        int64_t R, int budget, int32_t* __restrict__ out,
                                                         const WorkspaceHeader* __restrict__ hdr) {
   if (hdr != nullptr && hdr->error != 0) return;
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int64_t W4 = int64_t(budget) + 1;  // 16-byte chunks per row
-  for (int64_t row = int64_t(blockIdx.x) * warps + (threadIdx.x >> 5); row < T; row += int64_t(gridDim.x) * warps) {
+  for (int64_t i = int64_t(blockIdx.x) * warps + (threadIdx.x >> 5); i < R; i += int64_t(gridDim.x) * warps) {
+    const int64_t row = row_begin + i;
     const int b = seq_of_row(cu, S, row);
     const int t = int(row - __ldg(cu + b));
     const int e = (t + 1) >> 2, tail = (t + 1) & 3;
-    const int32_t* ids = pool_ids + row * budget;
-    int4* dst = reinterpret_cast<int4*>(out + row * (W4 * 4));
+    const int32_t* ids = pool_ids + i * budget;
+    int4* dst = reinterpret_cast<int4*>(out + i * (W4 * 4));
     for (int j = lane; j < budget; j += 32) {
       const int32_t id = __ldg(ids + j);
       dst[j] = (id >= 0 && id < e) ? make_int4(4 * id, 4 * id + 1, 4 * id + 2, 4 * id + 3)
@@ -73,16 +74,17 @@ __global__ void __launch_bounds__(256) expand_kernel_k4(const int32_t* __restric
 }
 
 __global__ void __launch_bounds__(256) expand_kernel_vec4(const int32_t* __restrict__ pool_ids,
-                                                          const int32_t* __restrict__ cu, int S, int64_t T,
-                                                          int kpool, int budget, int32_t* __restrict__ out,
+                                                          const int32_t* __restrict__ cu, int S, int64_t row_begin,
+                                                          int64_t R, int kpool, int budget,
+                                                          int32_t* __restrict__ out,
                                                           const WorkspaceHeader* __restrict__ hdr) {
   if (hdr != nullptr && hdr->error != 0) return;
   const int64_t W = int64_t(budget) * kpool + kpool;
   const int chunks = int(W / 4);
-  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
-    const RowInfo ri = row_info(cu, S, row, kpool);
-    const int32_t* ids = pool_ids + row * budget;
-    int4* dst = reinterpret_cast<int4*>(out + row * W);
+  for (int64_t i = blockIdx.x; i < R; i += gridDim.x) {
+    const RowInfo ri = row_info(cu, S, row_begin + i, kpool);
+    const int32_t* ids = pool_ids + i * budget;
+    int4* dst = reinterpret_cast<int4*>(out + i * W);
     for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
       const int64_t s0 = int64_t(c) * 4;
       const int64_t j = s0 / kpool;  // the 4 slots share one pool (kpool % 4 == 0)
@@ -98,41 +100,44 @@ __global__ void __launch_bounds__(256) expand_kernel_vec4(const int32_t* __restr
 }
 
 __global__ void __launch_bounds__(256) expand_kernel_scalar(const int32_t* __restrict__ pool_ids,
-                                                            const int32_t* __restrict__ cu, int S, int64_t T,
-                                                            int kpool, int budget, int32_t* __restrict__ out,
+                                                            const int32_t* __restrict__ cu, int S,
+                                                            int64_t row_begin, int64_t R, int kpool, int budget,
+                                                            int32_t* __restrict__ out,
                                                             const WorkspaceHeader* __restrict__ hdr) {
   if (hdr != nullptr && hdr->error != 0) return;
   const int64_t W = int64_t(budget) * kpool + kpool;
-  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
-    const RowInfo ri = row_info(cu, S, row, kpool);
-    const int32_t* ids = pool_ids + row * budget;
+  for (int64_t i = blockIdx.x; i < R; i += gridDim.x) {
+    const RowInfo ri = row_info(cu, S, row_begin + i, kpool);
+    const int32_t* ids = pool_ids + i * budget;
     for (int64_t s = threadIdx.x; s < W; s += blockDim.x) {
       const int64_t j = s / kpool;
       const int32_t pool = j < budget ? __ldg(ids + j) : -1;
-      out[row * W + s] = token_at(ri, pool, s, kpool, budget);
+      out[i * W + s] = token_at(ri, pool, s, kpool, budget);
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_expand(const int32_t* pool_ids, const int32_t* cu, int32_t S, int64_t T, int32_t kpool,
-                          int32_t budget, int32_t* out_tokens, const WorkspaceHeader* hdr, int num_sms,
-                          cudaStream_t stream) {
-  if (T == 0) return cudaSuccess;
-  int64_t blocks = T;
+cudaError_t launch_expand(const int32_t* pool_ids, const int32_t* cu, int32_t S, int64_t row_begin,
+                          int64_t row_end, int32_t kpool, int32_t budget, int32_t* out_tokens,
+                          const WorkspaceHeader* hdr, int num_sms, cudaStream_t stream) {
+  const int64_t R = row_end - row_begin;
+  if (R <= 0) return cudaSuccess;
+  int64_t blocks = R;
   const int64_t cap = int64_t(num_sms) * 16;
   if (blocks > cap) blocks = cap;
   const bool vec = (kpool % 4 == 0) && (reinterpret_cast<uintptr_t>(out_tokens) % 16 == 0);
   if (vec && kpool == 4) {
-    int64_t b4 = (T + 7) / 8;  // 8 rows (warps) per CTA
+    int64_t b4 = (R + 7) / 8;  // 8 rows (warps) per CTA
     if (b4 > int64_t(num_sms) * 16) b4 = int64_t(num_sms) * 16;
-    expand_kernel_k4<<<unsigned(b4), 256, 0, stream>>>(pool_ids, cu, S, T, budget, out_tokens, hdr);
+    expand_kernel_k4<<<unsigned(b4), 256, 0, stream>>>(pool_ids, cu, S, row_begin, R, budget, out_tokens, hdr);
   } else if (vec)
-    expand_kernel_vec4<<<unsigned(blocks), 256, 0, stream>>>(pool_ids, cu, S, T, kpool, budget, out_tokens, hdr);
+    expand_kernel_vec4<<<unsigned(blocks), 256, 0, stream>>>(pool_ids, cu, S, row_begin, R, kpool, budget,
+                                                              out_tokens, hdr);
   else
-    expand_kernel_scalar<<<unsigned(blocks), 256, 0, stream>>>(pool_ids, cu, S, T, kpool, budget, out_tokens,
-                                                                hdr);
+    expand_kernel_scalar<<<unsigned(blocks), 256, 0, stream>>>(pool_ids, cu, S, row_begin, R, kpool, budget,
+                                                                out_tokens, hdr);
   return cudaGetLastError();
 }
 

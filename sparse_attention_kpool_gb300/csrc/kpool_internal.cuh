@@ -108,9 +108,9 @@ inline cudaError_t record_stage_event(void* ev, cudaStream_t stream) {
 // Each returns cudaGetLastError() after enqueueing its kernel on `stream`.
 
 // K0: validates cu_seqlens, writes pool/item offsets and the heavy-first item
-// list; clears the header. One CTA.
-cudaError_t launch_plan(const int32_t* cu, int32_t S, int64_t T, int32_t kpool, char* ws,
-                        const WorkspaceLayout& L, cudaStream_t stream);
+// list of the rows [row_begin, row_end); clears the header. One CTA.
+cudaError_t launch_plan(const int32_t* cu, int32_t S, int64_t T, int32_t kpool, int64_t row_begin,
+                        int64_t row_end, char* ws, const WorkspaceLayout& L, cudaStream_t stream);
 
 // K1: pooled keys [P, d] into `out` (dtype elements).
 cudaError_t launch_pool(const void* k, kpool_dtype dtype, const int32_t* cu, int32_t S, int64_t T,
@@ -122,25 +122,29 @@ cudaError_t launch_pool_gated(const void* k, const float* gate, const float* ape
                               const int32_t* cu, int32_t S, int64_t T, int32_t d, int32_t kpool, void* out,
                               const char* ws, const WorkspaceLayout& L, int num_sms, cudaStream_t stream);
 
-// K2 (CUDA cores): any supported shape.
+// K2 (CUDA cores): any supported shape. Selects the global rows [row_begin, row_end);
+// output row i is global row row_begin + i.
 cudaError_t launch_select_simt(const void* q, const void* kp, const float* w, kpool_dtype dtype,
                                const int32_t* cu, int32_t S, int64_t T, int32_t H, int32_t d, int32_t kpool,
-                               int32_t budget, float scale, int32_t* out_ids, float* out_scores,
-                               char* ws, const WorkspaceLayout& L, int num_sms, cudaStream_t stream);
+                               int32_t budget, float scale, int64_t row_begin, int64_t row_end, int32_t* out_ids,
+                               float* out_scores, char* ws, const WorkspaceLayout& L, int num_sms,
+                               cudaStream_t stream);
 
-// K2 (tensor cores): bf16, H = 32, d = 128, budget <= 512.
+// K2 (tensor cores): bf16, H = 32, d = 128, budget <= 512. Works through the items the
+// planning kernel listed and writes the rows of [row_begin, row_end) only (row i of
+// the outputs is global row row_begin + i).
 bool select_tc_supported(kpool_dtype dtype, int32_t H, int32_t d, int32_t budget);
 cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, const int32_t* cu, int32_t S,
-                             int64_t T, int32_t kpool, int32_t budget, float scale, int32_t* out_ids,
-                             float* out_scores, char* ws, const WorkspaceLayout& L, int grid,
-                             cudaStream_t stream);
+                             int64_t T, int32_t kpool, int32_t budget, float scale, int64_t row_begin,
+                             int64_t row_end, int32_t* out_ids, float* out_scores, char* ws,
+                             const WorkspaceLayout& L, int grid, cudaStream_t stream);
 
-// K3: pool ids -> token ids.
-// `hdr` may be null; when given, the kernel does nothing if the planning
-// kernel recorded an error.
-cudaError_t launch_expand(const int32_t* pool_ids, const int32_t* cu, int32_t S, int64_t T, int32_t kpool,
-                          int32_t budget, int32_t* out_tokens, const WorkspaceHeader* hdr, int num_sms,
-                          cudaStream_t stream);
+// K3: pool ids -> token ids for the global rows [row_begin, row_end) (pool_ids and
+// out_tokens hold those rows only). `hdr` may be null; when given, the kernel does
+// nothing if the planning kernel recorded an error.
+cudaError_t launch_expand(const int32_t* pool_ids, const int32_t* cu, int32_t S, int64_t row_begin,
+                          int64_t row_end, int32_t kpool, int32_t budget, int32_t* out_tokens,
+                          const WorkspaceHeader* hdr, int num_sms, cudaStream_t stream);
 
 // Selection for explicit query rows against an existing pooled-key cache
 // (kpool_rows.cu): workspace layout, shape support and the R0-R2 launches.
@@ -155,6 +159,18 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
                                int32_t budget, float scale, int32_t* out_ids, float* out_scores,
                                int32_t* out_tokens, char* ws, const RowsLayout& L, int num_sms, int max_ctas,
                                cudaStream_t stream, void* const* stage_events);
+
+// Every check kpool_select_ex / kpool_select_pooled make before the workspace's:
+// options, shape, the row range, pointers and alignment, kernel support (kin is k,
+// or the pooled keys). On KPOOL_OK, *use_tc says which score kernel runs and
+// [*row_begin, *row_end) which global rows are selected ([0, T) without a row
+// range); T = 0 or an empty range passes and needs no further work.
+kpool_status select_check_args(const void* q, const void* kin, const float* w, const int32_t* cu_seqlens,
+                               int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                               kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
+                               const int32_t* out_pool_ids, const int32_t* out_token_ids,
+                               const float* out_pool_scores, const kpool_options* options, bool* use_tc,
+                               int64_t* row_begin, int64_t* row_end);
 
 // Bounded-wait self test.
 cudaError_t launch_wait_selftest(char* ws, int64_t spin_limit, cudaStream_t stream);

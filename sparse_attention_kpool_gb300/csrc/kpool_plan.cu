@@ -8,7 +8,9 @@
 //   * writes the first pooled-key row of every sequence, pool_off[b] =
 //     sum_{j<b} floor(L_j / kpool) (tp.rs module docs: n_pools = seq / kpool);
 //   * lists the work items of the tensor-core kernel: one item per block of
-//     kItemRows query rows of one sequence, ordered deepest-first. An item at
+//     kItemRows query rows of one sequence that holds rows of the call's row
+//     range (every row unless the caller selects a shard of rows), ordered
+//     deepest-first. An item at
 //     depth j (local rows j*kItemRows ...) scores about j*kItemRows/kpool pools
 //     under the causal window, so deepest-first is heaviest-first and the
 //     persistent kernel's static round-robin stays balanced;
@@ -48,8 +50,18 @@ __device__ int block_inclusive_scan(int v, int* total, int* s_warp) {
   return res;
 }
 
+// Item blocks [j_lo, j_hi) of a sequence starting at global row c0 with `len` rows that
+// hold rows of the range [row_begin, row_end) (empty when none does).
+__device__ __forceinline__ int2 item_range(int64_t c0, int len, int64_t row_begin, int64_t row_end) {
+  const int64_t lo = min(max(row_begin - c0, int64_t(0)), int64_t(len));
+  const int64_t hi = min(max(row_end - c0, int64_t(0)), int64_t(len));
+  if (lo >= hi) return make_int2(0, 0);
+  return make_int2(int(lo / kItemRows), int((hi + kItemRows - 1) / kItemRows));
+}
+
 __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restrict__ cu, int S, int64_t T,
-                                                        int kpool, WorkspaceHeader* hdr, int32_t* pool_off,
+                                                        int kpool, int64_t row_begin, int64_t row_end,
+                                                        WorkspaceHeader* hdr, int32_t* pool_off,
                                                         int32_t* qblk_off, int32_t* level_cnt,
                                                         int32_t* level_start, int32_t* level_fill,
                                                         int2* items, int64_t max_levels) {
@@ -76,7 +88,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     return;
   }
 
-  // pool and item offsets (exclusive scans over sequences)
+  // pool and item offsets (exclusive scans over sequences); a sequence's items are the
+  // blocks of kItemRows rows that hold rows of [row_begin, row_end)
   int carry_p = 0, carry_q = 0;
   for (int base = 0; base < S; base += kThreads) {
     const int b = base + tid;
@@ -84,8 +97,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     if (b < S) {
       const int len = cu[b + 1] - cu[b];
       np = len / kpool;
-      nq = (len + kItemRows - 1) / kItemRows;
-      atomicMax(&s_max_depth, nq);
+      const int2 jr = item_range(cu[b], len, row_begin, row_end);
+      nq = jr.y - jr.x;
+      atomicMax(&s_max_depth, jr.y);
     }
     int tp, tq;
     const int ip = block_inclusive_scan(np, &tp, s_warp);
@@ -99,12 +113,12 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
   }
   __syncthreads();
   const int n_items = carry_q;
-  const int n_levels = s_max_depth;
+  const int n_levels = s_max_depth;  // item depths 0 .. n_levels - 1
   if (tid == 0) {
     pool_off[S] = carry_p;
     qblk_off[S] = carry_q;
   }
-  if (n_levels > max_levels) {  // cannot happen with a workspace sized for T
+  if (int64_t(n_levels) + 1 > max_levels) {  // cannot happen with a workspace sized for T
     if (tid == 0) {
       hdr->error = KPOOL_ERR_WORKSPACE;
       hdr->n_items = 0;
@@ -115,33 +129,41 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
     return;
   }
 
-  // level_cnt[j] = number of sequences with exactly j+1 items
-  for (int j = tid; j < n_levels; j += kThreads) {
+  // level_cnt: +1 at each sequence's first item depth, -1 past its last, so its
+  // prefix sum is the number of items at each depth
+  for (int j = tid; j <= n_levels; j += kThreads) {
     level_cnt[j] = 0;
     level_fill[j] = 0;
   }
   __syncthreads();
   for (int b = tid; b < S; b += kThreads) {
-    const int nq = (cu[b + 1] - cu[b] + kItemRows - 1) / kItemRows;
-    if (nq > 0) atomicAdd(&level_cnt[nq - 1], 1);
+    const int2 jr = item_range(cu[b], cu[b + 1] - cu[b], row_begin, row_end);
+    if (jr.y > jr.x) {
+      atomicAdd(&level_cnt[jr.x], 1);
+      atomicAdd(&level_cnt[jr.y], -1);
+    }
   }
   __syncthreads();
-
-  // deep[j] = #sequences with more than j items (suffix sum of level_cnt);
-  // level_start[j] = sum_{j' > j} deep[j'] (deeper levels come first).
-  int carry_deep = 0, carry_start = 0;
+  int carry = 0;
   for (int base = 0; base < n_levels; base += kThreads) {
-    const int r = base + tid;           // r-th level from the deepest
-    const int j = n_levels - 1 - r;
-    const int c = (r < n_levels) ? level_cnt[j] : 0;
+    const int j = base + tid;
+    const int dv = j < n_levels ? level_cnt[j] : 0;
     int tot;
-    const int deep = carry_deep + block_inclusive_scan(c, &tot, s_warp);
-    carry_deep += tot;
-    const int d = (r < n_levels) ? deep : 0;
-    int tot2;
-    const int incl = block_inclusive_scan(d, &tot2, s_warp);
-    if (r < n_levels) level_start[j] = carry_start + incl - d;
-    carry_start += tot2;
+    const int incl = block_inclusive_scan(dv, &tot, s_warp);
+    if (j < n_levels) level_cnt[j] = carry + incl;  // items at depth j
+    carry += tot;
+  }
+  __syncthreads();
+  // level_start[j] = items at depths deeper than j (deeper levels come first)
+  carry = 0;
+  for (int base = 0; base < n_levels; base += kThreads) {
+    const int r = base + tid;  // r-th level from the deepest
+    const int j = n_levels - 1 - r;
+    const int c = r < n_levels ? level_cnt[j] : 0;
+    int tot;
+    const int incl = block_inclusive_scan(c, &tot, s_warp);
+    if (r < n_levels) level_start[j] = carry + incl - c;
+    carry += tot;
   }
   __syncthreads();
 
@@ -152,7 +174,8 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
       const int mid = (lo + hi + 1) >> 1;
       if (qblk_off[mid] <= i) lo = mid; else hi = mid - 1;
     }
-    const int j = i - qblk_off[lo];
+    const int2 jr = item_range(cu[lo], cu[lo + 1] - cu[lo], row_begin, row_end);
+    const int j = jr.x + (i - qblk_off[lo]);
     const int pos = level_start[j] + atomicAdd(&level_fill[j], 1);
     items[pos] = make_int2(lo, j);
   }
@@ -167,10 +190,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const int32_t* __restric
 
 }  // namespace
 
-cudaError_t launch_plan(const int32_t* cu, int32_t S, int64_t T, int32_t kpool, char* ws,
-                        const WorkspaceLayout& L, cudaStream_t stream) {
+cudaError_t launch_plan(const int32_t* cu, int32_t S, int64_t T, int32_t kpool, int64_t row_begin,
+                        int64_t row_end, char* ws, const WorkspaceLayout& L, cudaStream_t stream) {
   plan_kernel<<<1, kThreads, 0, stream>>>(
-      cu, S, T, kpool, reinterpret_cast<WorkspaceHeader*>(ws + L.header),
+      cu, S, T, kpool, row_begin, row_end, reinterpret_cast<WorkspaceHeader*>(ws + L.header),
       reinterpret_cast<int32_t*>(ws + L.pool_off), reinterpret_cast<int32_t*>(ws + L.qblk_off),
       reinterpret_cast<int32_t*>(ws + L.level_cnt), reinterpret_cast<int32_t*>(ws + L.level_start),
       reinterpret_cast<int32_t*>(ws + L.level_fill), reinterpret_cast<int2*>(ws + L.items), L.max_levels);

@@ -30,7 +30,7 @@ template <typename T, bool kNegScale>
 __global__ void __launch_bounds__(128) select_simt_kernel(
     const T* __restrict__ q, const T* __restrict__ kp, const float* __restrict__ w,
     const int32_t* __restrict__ cu, const int32_t* __restrict__ pool_off, const WorkspaceHeader* __restrict__ hdr,
-    int S, int64_t T_total, int H, int d, int kpool, int budget, int cap, float abs_scale,
+    int S, int64_t row_begin, int64_t row_end, int H, int d, int kpool, int budget, int cap, float abs_scale,
     int32_t* __restrict__ out_ids, float* __restrict__ out_scores) {
   extern __shared__ uint64_t smem_keys[];
   if (hdr->error != 0) return;
@@ -40,7 +40,9 @@ __global__ void __launch_bounds__(128) select_simt_kernel(
   uint64_t* buf = smem_keys + size_t(warp) * cap;
   const unsigned lt_mask = (1u << lane) - 1u;
 
-  for (int64_t row = int64_t(blockIdx.x) * warps + warp; row < T_total; row += int64_t(gridDim.x) * warps) {
+  for (int64_t row = row_begin + int64_t(blockIdx.x) * warps + warp; row < row_end;
+       row += int64_t(gridDim.x) * warps) {
+    const int64_t orow = row - row_begin;  // output row
     const int b = seq_of_row(cu, S, row);
     const int64_t t = row - __ldg(cu + b);
     const int64_t eligible = (t + 1) / kpool;
@@ -85,8 +87,8 @@ __global__ void __launch_bounds__(128) select_simt_kernel(
     warp_sort_desc(buf, cap);
     for (int j = lane; j < budget; j += 32) {
       const uint64_t key = buf[j];
-      out_ids[row * budget + j] = key ? int32_t(key_pool(key)) : -1;
-      if (out_scores) out_scores[row * budget + j] = key ? key_score(key) : -INFINITY;
+      out_ids[orow * budget + j] = key ? int32_t(key_pool(key)) : -1;
+      if (out_scores) out_scores[orow * budget + j] = key ? key_score(key) : -INFINITY;
     }
     __syncwarp();
   }
@@ -99,10 +101,10 @@ int simt_capacity(int budget) {
 }
 
 template <typename Elem, bool kNeg>
-cudaError_t launch_typed(const void* q, const void* kp, const float* w, const int32_t* cu, int32_t S, int64_t T,
-                         int32_t H, int32_t d, int32_t kpool, int32_t budget, float abs_scale, int32_t* out_ids,
-                         float* out_scores, const char* ws, const WorkspaceLayout& L, int num_sms,
-                         cudaStream_t stream) {
+cudaError_t launch_typed(const void* q, const void* kp, const float* w, const int32_t* cu, int32_t S,
+                         int64_t row_begin, int64_t row_end, int32_t H, int32_t d, int32_t kpool, int32_t budget,
+                         float abs_scale, int32_t* out_ids, float* out_scores, const char* ws,
+                         const WorkspaceLayout& L, int num_sms, cudaStream_t stream) {
   const int cap = simt_capacity(budget);
   const size_t per_warp = size_t(cap) * sizeof(uint64_t);
   int warps = int((96 * 1024) / per_warp);
@@ -114,13 +116,13 @@ cudaError_t launch_typed(const void* q, const void* kp, const float* w, const in
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
   }
-  int64_t blocks = (T + warps - 1) / warps;
+  int64_t blocks = (row_end - row_begin + warps - 1) / warps;
   const int64_t cap_blocks = int64_t(num_sms) * 16;
   if (blocks > cap_blocks) blocks = cap_blocks;
   kern<<<unsigned(blocks), warps * 32, smem, stream>>>(
       static_cast<const Elem*>(q), static_cast<const Elem*>(kp), w, cu, reinterpret_cast<const int32_t*>(ws + L.pool_off),
-      reinterpret_cast<const WorkspaceHeader*>(ws + L.header), S, T, H, d, kpool, budget, cap, abs_scale, out_ids,
-      out_scores);
+      reinterpret_cast<const WorkspaceHeader*>(ws + L.header), S, row_begin, row_end, H, d, kpool, budget, cap,
+      abs_scale, out_ids, out_scores);
   return cudaGetLastError();
 }
 
@@ -128,20 +130,21 @@ cudaError_t launch_typed(const void* q, const void* kp, const float* w, const in
 
 cudaError_t launch_select_simt(const void* q, const void* kp, const float* w, kpool_dtype dtype, const int32_t* cu,
                                int32_t S, int64_t T, int32_t H, int32_t d, int32_t kpool, int32_t budget, float scale,
-                               int32_t* out_ids, float* out_scores, char* ws, const WorkspaceLayout& L, int num_sms,
-                               cudaStream_t stream) {
-  if (T == 0 || budget == 0) return cudaSuccess;
+                               int64_t row_begin, int64_t row_end, int32_t* out_ids, float* out_scores, char* ws,
+                               const WorkspaceLayout& L, int num_sms, cudaStream_t stream) {
+  if (T == 0 || budget == 0 || row_end <= row_begin) return cudaSuccess;
   const bool neg = scale < 0.0f;
   const float abs_scale = neg ? -scale : scale;
+  const int64_t rb = row_begin, re = row_end;
   if (dtype == KPOOL_BF16)
-    return neg ? launch_typed<__nv_bfloat16, true>(q, kp, w, cu, S, T, H, d, kpool, budget, abs_scale, out_ids,
+    return neg ? launch_typed<__nv_bfloat16, true>(q, kp, w, cu, S, rb, re, H, d, kpool, budget, abs_scale, out_ids,
                                                     out_scores, ws, L, num_sms, stream)
-               : launch_typed<__nv_bfloat16, false>(q, kp, w, cu, S, T, H, d, kpool, budget, abs_scale, out_ids,
+               : launch_typed<__nv_bfloat16, false>(q, kp, w, cu, S, rb, re, H, d, kpool, budget, abs_scale, out_ids,
                                                      out_scores, ws, L, num_sms, stream);
-  return neg ? launch_typed<float, true>(q, kp, w, cu, S, T, H, d, kpool, budget, abs_scale, out_ids, out_scores,
+  return neg ? launch_typed<float, true>(q, kp, w, cu, S, rb, re, H, d, kpool, budget, abs_scale, out_ids, out_scores,
                                          ws, L, num_sms, stream)
-             : launch_typed<float, false>(q, kp, w, cu, S, T, H, d, kpool, budget, abs_scale, out_ids, out_scores,
-                                          ws, L, num_sms, stream);
+             : launch_typed<float, false>(q, kp, w, cu, S, rb, re, H, d, kpool, budget, abs_scale, out_ids,
+                                          out_scores, ws, L, num_sms, stream);
 }
 
 }  // namespace kpool

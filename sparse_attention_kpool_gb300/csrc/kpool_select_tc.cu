@@ -415,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const float* __restrict__ w, const int32_t* __restrict__ cu,
                      const int32_t* __restrict__ pool_off, const int2* __restrict__ items,
                      WorkspaceHeader* __restrict__ hdr, int kpool, int budget, float abs_scale,
-                     int32_t* __restrict__ out_ids, float* __restrict__ out_scores) {
+                     int64_t row_begin, int64_t row_end, int32_t* __restrict__ out_ids,
+                     float* __restrict__ out_scores) {
   // Pointers derived directly from the __shared__ array keep the shared address
   // space, so the compiler emits shared loads, stores and atomics (LDS/STS/ATOMS)
   // rather than generic ones.
@@ -646,8 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = rbase + j;
         const int32_t* c = s_count + q * 4;
         const int n = c[0] + c[1] + c[2] + c[3];
+        const int64_t grow = it.seq_start + it.t0 + q;
+        const bool written = grow >= row_begin && grow < row_end;  // rows past the sequence have n = 0
         // the sort below reads the first kFinalChunk slots of each region
-        if (n > budget || max(max(c[0], c[1]), max(c[2], c[3])) > kFinalChunk) {
+        if (written && (n > budget || max(max(c[0], c[1]), max(c[2], c[3])) > kFinalChunk)) {
           compact_row(s_cand + q * kCap, s_count + q * 4, budget, 0, gt, bar_id, sel, nullptr);
         }
       }
@@ -655,10 +658,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int q = rbase + wq;
         const int row = it.t0 + q;
-        if (row < it.len) {
-          const int64_t grow = it.seq_start + row;
-          rank_and_write_row(s_cand + q * kCap, s_count + q * 4, budget, out_ids + grow * budget,
-                             out_scores ? out_scores + grow * budget : nullptr);
+        const int64_t grow = it.seq_start + row;
+        if (row < it.len && grow >= row_begin && grow < row_end) {  // items may straddle the row range
+          const int64_t orow = grow - row_begin;
+          rank_and_write_row(s_cand + q * kCap, s_count + q * 4, budget, out_ids + orow * budget,
+                             out_scores ? out_scores + orow * budget : nullptr);
           __syncwarp();
         }
       }
@@ -717,10 +721,11 @@ bool select_tc_supported(kpool_dtype dtype, int32_t H, int32_t d, int32_t budget
 }
 
 cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, const int32_t* cu, int32_t S, int64_t T,
-                             int32_t kpool, int32_t budget, float scale, int32_t* out_ids, float* out_scores,
-                             char* ws, const WorkspaceLayout& L, int grid, cudaStream_t stream) {
+                             int32_t kpool, int32_t budget, float scale, int64_t row_begin, int64_t row_end,
+                             int32_t* out_ids, float* out_scores, char* ws, const WorkspaceLayout& L, int grid,
+                             cudaStream_t stream) {
   (void)S;
-  if (T == 0) return cudaSuccess;
+  if (T == 0 || row_end <= row_begin) return cudaSuccess;
   if (T * kHeads > int64_t(INT32_MAX)) return cudaErrorInvalidValue;
   CUtensorMap map_q, map_kp;
   if (!make_map(&map_q, q, uint64_t(T) * kHeads, kN)) return cudaErrorInvalidValue;
@@ -740,7 +745,7 @@ cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, cons
   kern<<<grid, kThreads, kSmemBytes, stream>>>(
       map_q, map_kp, w, cu, reinterpret_cast<const int32_t*>(ws + L.pool_off),
       reinterpret_cast<const int2*>(ws + L.items), reinterpret_cast<WorkspaceHeader*>(ws + L.header), kpool, budget,
-      abs_scale, out_ids, out_scores);
+      abs_scale, row_begin, row_end, out_ids, out_scores);
   return cudaGetLastError();
 }
 

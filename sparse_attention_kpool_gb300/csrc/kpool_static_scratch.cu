@@ -10,9 +10,11 @@
 // GPU loading this library holds until the process exits.
 //
 // Rules (also stated in include/kpool.h):
-//   * capacity: KPOOL_STATIC_SCRATCH_BYTES; a call whose workspace requirement
-//     (kpool_workspace_bytes) exceeds it is rejected with KPOOL_ERR_WORKSPACE
-//     before any GPU work;
+//   * the arguments are checked exactly as kpool_select checks them (a shape the
+//     kernels do not implement is KPOOL_ERR_UNSUPPORTED, whatever its size); only
+//     then is the capacity checked: a call whose workspace requirement
+//     (kpool_workspace_bytes) exceeds KPOOL_STATIC_SCRATCH_BYTES is rejected with
+//     KPOOL_ERR_WORKSPACE, before any GPU work;
 //   * the first call on a device looks up the array's device address with that
 //     device current (cudaGetSymbolAddress) and caches it; make that first call
 //     before any stream capture;
@@ -20,7 +22,9 @@
 //     GPU (different streams, different host threads) race -- serialise them;
 //   * nothing here allocates: no cudaMalloc, cudaFree or allocating library call;
 //   * the array keeps the previous call's contents; the planning kernel rewrites
-//     every field the later kernels read, so nothing needs clearing up front.
+//     every field the later kernels read, so nothing needs clearing up front;
+//   * errors found on the device land in the array's header, read back with
+//     kpool_static_scratch_last_device_error.
 #include <atomic>
 
 #include <cuda_runtime.h>
@@ -60,9 +64,12 @@ extern "C" kpool_status kpool_select_static_scratch(const void* q, const void* k
                                                     kpool_dtype dtype, int32_t kpool, int32_t index_topk, float scale,
                                                     int32_t* out_pool_ids, int32_t* out_token_ids,
                                                     float* out_pool_scores, void* stream) {
-  if (total_tokens == 0)
-    return kpool_select(q, k, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool, index_topk,
-                        scale, out_pool_ids, out_token_ids, out_pool_scores, nullptr, 0, stream);
+  bool use_tc = false;
+  int64_t rb = 0, re = 0;
+  const kpool_status st = kpool::select_check_args(q, k, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim,
+                                                   dtype, kpool, index_topk, scale, out_pool_ids, out_token_ids,
+                                                   out_pool_scores, nullptr, &use_tc, &rb, &re);
+  if (st != KPOOL_OK || total_tokens == 0) return st;
   const size_t need = kpool_workspace_bytes(total_tokens, num_seqs, heads, head_dim, dtype, kpool, index_topk);
   if (need == 0) return KPOOL_ERR_INVALID_ARG;
   if (need > kScratchBytes) return KPOOL_ERR_WORKSPACE;
@@ -70,4 +77,10 @@ extern "C" kpool_status kpool_select_static_scratch(const void* q, const void* k
   if (scratch_address(&scratch) != cudaSuccess) return KPOOL_ERR_CUDA;
   return kpool_select(q, k, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool, index_topk,
                       scale, out_pool_ids, out_token_ids, out_pool_scores, scratch, kScratchBytes, stream);
+}
+
+extern "C" kpool_status kpool_static_scratch_last_device_error(void* stream) {
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return KPOOL_ERR_CUDA;
+  return kpool_last_device_error(scratch, stream);
 }

@@ -39,7 +39,8 @@ EXPORTED = (
     "kpool_workspace_bytes", "kpool_select", "kpool_select_ex", "kpool_pool_keys", "kpool_expand",
     "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string", "kpool_last_cuda_error",
     "kpool_select_static_scratch", "kpool_rows_workspace_bytes", "kpool_select_rows", "kpool_select_rows_ex",
-    "kpool_pool_keys_gated", "kpool_select_pooled",
+    "kpool_pool_keys_gated", "kpool_select_pooled", "kpool_static_scratch_last_device_error",
+    "kpool_balanced_row_split",
 )
 KPOOL_STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -51,9 +52,13 @@ class KpoolError(RuntimeError):
         super().__init__(f"{what}: {kpool_status_string(status)} (status {status}){detail}")
 
 
+KPOOL_OPT_ROW_RANGE = 1
+
+
 class kpool_options(ctypes.Structure):
     _fields_ = [("score_kernel", ctypes.c_int32), ("max_ctas", ctypes.c_int32),
-                ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("reserved", ctypes.c_int32 * 4)]
+                ("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("row_begin", ctypes.c_int32),
+                ("row_end", ctypes.c_int32), ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -96,6 +101,8 @@ def load() -> ctypes.CDLL:
         lib.kpool_last_cuda_error.restype = ctypes.c_char_p
         lib.kpool_select_static_scratch.argtypes = [P, P, P, P, i32, i64, i32, i32, i32, i32, i32, f32, P, P, P, P]
         lib.kpool_select_static_scratch.restype = i32
+        lib.kpool_static_scratch_last_device_error.argtypes = [P]
+        lib.kpool_static_scratch_last_device_error.restype = i32
         lib.kpool_rows_workspace_bytes.argtypes = [i32, i64, i32, i32, i32]
         lib.kpool_rows_workspace_bytes.restype = sz
         lib.kpool_select_rows.argtypes = [P, P, P, P, i32, P, P, i32, i64, i32, i32, i32, i32, i32, f32, P, P, P,
@@ -107,6 +114,8 @@ def load() -> ctypes.CDLL:
         lib.kpool_pool_keys_gated.restype = i32
         lib.kpool_select_pooled.argtypes = sel + [ctypes.POINTER(kpool_options)]
         lib.kpool_select_pooled.restype = i32
+        lib.kpool_balanced_row_split.argtypes = [P, i32, i32, i64, i32, P]
+        lib.kpool_balanced_row_split.restype = i32
         _lib = lib
         return lib
 
@@ -161,9 +170,10 @@ def new_workspace(total_tokens: int, num_seqs: int, heads: int, head_dim: int, d
 def kpool_select_ex(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor, kpool: int,
                     index_topk: int, scale: float, out_pool_ids=None, out_token_ids=None, out_pool_scores=None,
                     return_scores: bool = False, workspace=None, stream=None, score_kernel: int = KPOOL_SCORE_AUTO,
-                    max_ctas: int = 0, stage_events=None):
-    """q [T,H,d], k [T,d] (bf16 or fp32), w [T,H] fp32, cu_seqlens [S+1] int32 -> (pool_ids [T,B],
-    token_ids [T, index_topk+kpool], pool_scores [T,B] or None).
+                    max_ctas: int = 0, stage_events=None, row_range=None):
+    """q [T,H,d], k [T,d] (bf16 or fp32), w [T,H] fp32, cu_seqlens [S+1] int32 -> (pool_ids [R,B],
+    token_ids [R, index_topk+kpool], pool_scores [R,B] or None), R = T rows, or the rows of
+    row_range = (row_begin, row_end) (a shard of query rows; no scores on that path).
 
     stage_events: optional 5 already-recorded torch.cuda.Event(enable_timing=True); the library
     re-records them around its four kernels (see kpool_options in kpool.h)."""
@@ -173,17 +183,21 @@ def kpool_select_ex(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, cu_seqlen
     if k.dtype != q.dtype or w.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
         raise TypeError("k must match q's dtype; w must be float32; cu_seqlens int32")
     B = index_topk // kpool if kpool > 0 else 0
+    R = T if row_range is None else max(0, int(row_range[1]) - int(row_range[0]))
     dev = q.device
     if out_pool_ids is None:
-        out_pool_ids = torch.empty((T, B), dtype=torch.int32, device=dev)
+        out_pool_ids = torch.empty((R, B), dtype=torch.int32, device=dev)
     if out_token_ids is None:
-        out_token_ids = torch.empty((T, index_topk + kpool), dtype=torch.int32, device=dev)
+        out_token_ids = torch.empty((R, index_topk + kpool), dtype=torch.int32, device=dev)
     if out_pool_scores is None and return_scores:
-        out_pool_scores = torch.empty((T, B), dtype=torch.float32, device=dev)
+        out_pool_scores = torch.empty((R, B), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = new_workspace(T, S, H, d, dt, kpool, index_topk, dev)
     _check_cuda(q, k, w, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores, workspace)
     opts = kpool_options(score_kernel, max_ctas)
+    if row_range is not None:
+        opts.row_begin, opts.row_end = int(row_range[0]), int(row_range[1])
+        opts.flags = KPOOL_OPT_ROW_RANGE
     if stage_events is not None:
         if len(stage_events) != 5:
             raise ValueError("stage_events needs 5 events")
@@ -271,6 +285,11 @@ def kpool_select_static_scratch(q: torch.Tensor, k: torch.Tensor, w: torch.Tenso
     return out_pool_ids, out_token_ids, out_pool_scores
 
 
+def kpool_static_scratch_last_device_error(stream=None) -> int:
+    """Device error word of the last kpool_select_static_scratch call on this device (syncs)."""
+    return int(load().kpool_static_scratch_last_device_error(_stream(stream)))
+
+
 def kpool_rows_workspace_bytes(num_rows: int, total_tokens: int, num_seqs: int, kpool: int, index_topk: int) -> int:
     return int(load().kpool_rows_workspace_bytes(num_rows, total_tokens, num_seqs, kpool, index_topk))
 
@@ -356,25 +375,30 @@ def kpool_pool_keys_gated(k: torch.Tensor, gate: torch.Tensor, ape: torch.Tensor
 def kpool_select_pooled(q: torch.Tensor, pooled_keys: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor,
                         kpool: int, index_topk: int, scale: float, out_pool_ids=None, out_token_ids=None,
                         out_pool_scores=None, return_scores: bool = False, workspace=None, stream=None,
-                        score_kernel: int = KPOOL_SCORE_AUTO, max_ctas: int = 0):
-    """Selection from pooled keys the caller already has (steps 2-4); q [T,H,d], pooled_keys [>= P, d]."""
+                        score_kernel: int = KPOOL_SCORE_AUTO, max_ctas: int = 0, row_range=None):
+    """Selection from pooled keys the caller already has (steps 2-4); q [T,H,d], pooled_keys [>= P, d].
+    row_range as for kpool_select_ex."""
     T, H, d = q.shape
     S = cu_seqlens.numel() - 1
     dt = _dtype_code(q)
     if pooled_keys.dtype != q.dtype or w.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
         raise TypeError("pooled_keys must match q's dtype; w must be float32; cu_seqlens int32")
     B = index_topk // kpool if kpool > 0 else 0
+    R = T if row_range is None else max(0, int(row_range[1]) - int(row_range[0]))
     dev = q.device
     if out_pool_ids is None:
-        out_pool_ids = torch.empty((T, B), dtype=torch.int32, device=dev)
+        out_pool_ids = torch.empty((R, B), dtype=torch.int32, device=dev)
     if out_token_ids is None:
-        out_token_ids = torch.empty((T, index_topk + kpool), dtype=torch.int32, device=dev)
+        out_token_ids = torch.empty((R, index_topk + kpool), dtype=torch.int32, device=dev)
     if out_pool_scores is None and return_scores:
-        out_pool_scores = torch.empty((T, B), dtype=torch.float32, device=dev)
+        out_pool_scores = torch.empty((R, B), dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = new_workspace(T, S, H, d, dt, kpool, index_topk, dev)
     _check_cuda(q, pooled_keys, w, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores, workspace)
     opts = kpool_options(score_kernel, max_ctas)
+    if row_range is not None:
+        opts.row_begin, opts.row_end = int(row_range[0]), int(row_range[1])
+        opts.flags = KPOOL_OPT_ROW_RANGE
     st = load().kpool_select_pooled(_ptr(q), _ptr(pooled_keys), _ptr(w), _ptr(cu_seqlens), S, T, H, d, dt, kpool,
                                     index_topk, float(scale), _ptr(out_pool_ids), _ptr(out_token_ids),
                                     _ptr(out_pool_scores), _ptr(workspace), workspace.numel(), _stream(stream),
@@ -382,3 +406,17 @@ def kpool_select_pooled(q: torch.Tensor, pooled_keys: torch.Tensor, w: torch.Ten
     if st != KPOOL_OK:
         raise KpoolError(st, "kpool_select_pooled")
     return out_pool_ids, out_token_ids, out_pool_scores
+
+
+def kpool_balanced_row_split(cu_seqlens, kpool: int, parts: int, row_weight: int = 0) -> list:
+    """Bounds [b0=0, b1, ..., b_parts=T] of `parts` contiguous row ranges of near-equal work
+    (causal pairs + row_weight per row); cu_seqlens on the host (list, numpy or CPU tensor)."""
+    import numpy as np
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens if not torch.is_tensor(cu_seqlens) else cu_seqlens.cpu(),
+                                         dtype=np.int32))
+    out = np.zeros(int(parts) + 1, dtype=np.int32)
+    st = load().kpool_balanced_row_split(cu.ctypes.data_as(ctypes.c_void_p), len(cu) - 1, int(kpool),
+                                         int(row_weight), int(parts), out.ctypes.data_as(ctypes.c_void_p))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_balanced_row_split")
+    return [int(x) for x in out]

@@ -6,6 +6,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 from sparse_attention_kpool_gb300 import build as kbuild
@@ -96,7 +97,10 @@ def test_select_rejects_bad_arguments(lib):
     assert _select(lib, ws=FAKE + 64) == K.KPOOL_ERR_WORKSPACE     # 256-byte alignment
     assert _select(lib, ws_bytes=1024) == K.KPOOL_ERR_WORKSPACE
     bad = K.kpool_options(K.KPOOL_SCORE_AUTO, 0)
-    bad.reserved[3] = 1
+    bad.reserved = 1
+    assert _select(lib, opts=bad) == K.KPOOL_ERR_INVALID_ARG
+    bad = K.kpool_options(K.KPOOL_SCORE_AUTO, 0)
+    bad.flags = 2  # unknown flag
     assert _select(lib, opts=bad) == K.KPOOL_ERR_INVALID_ARG
     assert _select(lib, opts=K.kpool_options(9, 0)) == K.KPOOL_ERR_INVALID_ARG
     assert _select(lib, opts=K.kpool_options(0, -1)) == K.KPOOL_ERR_INVALID_ARG
@@ -208,3 +212,73 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(K, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         K.load()
+
+
+def _range_opts(b, e, flags=K.KPOOL_OPT_ROW_RANGE):
+    o = K.kpool_options(K.KPOOL_SCORE_AUTO, 0)
+    o.row_begin, o.row_end, o.flags = b, e, flags
+    return o
+
+
+def test_row_range_validation(lib):
+    # bounds: 0 <= row_begin <= row_end <= T
+    assert _select(lib, T=64, opts=_range_opts(-1, 10)) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, T=64, opts=_range_opts(10, 9)) == K.KPOOL_ERR_INVALID_ARG
+    assert _select(lib, T=64, opts=_range_opts(10, 65)) == K.KPOOL_ERR_INVALID_ARG
+    # a range without the flag is a mistake, not a silent whole-batch call
+    assert _select(lib, T=64, opts=_range_opts(0, 10, flags=0)) == K.KPOOL_ERR_INVALID_ARG
+    # the sharded path returns no index scores (the pages reject that combination)
+    assert _select(lib, T=64, scores=FAKE, opts=_range_opts(0, 32)) == K.KPOOL_ERR_INVALID_ARG
+    # an empty range is a valid no-op, even with null outputs
+    assert _select(lib, T=64, ids=0, toks=0, ws=0, opts=_range_opts(17, 17)) == K.KPOOL_OK
+    # a valid range still checks the workspace
+    assert _select(lib, T=64, ws=0, opts=_range_opts(0, 32)) == K.KPOOL_ERR_WORKSPACE
+    # the decode-rows entry point takes no row range
+    P = ctypes.c_void_p
+    o = _range_opts(0, 1)
+    assert lib.kpool_select_rows_ex(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1, P(FAKE), P(FAKE), 1, 64, 32, 128,
+                                    K.KPOOL_BF16, 4, 16, 0.5, P(FAKE), P(FAKE), None, P(FAKE), 1 << 30, None,
+                                    ctypes.byref(o)) == K.KPOOL_ERR_INVALID_ARG
+
+
+def _pairs_per_row(cu, kpool):
+    rows = []
+    for b in range(len(cu) - 1):
+        rows += [(t + 1) // kpool for t in range(cu[b + 1] - cu[b])]
+    return np.array(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("seqlens,kpool,parts,row_weight", [
+    ((524288,), 4, 8, 0), ((131072,), 4, 3, 512), ((8192, 16384, 3072, 5120), 4, 8, 0),
+    ((5, 0, 130, 1027, 3), 3, 4, 0), ((1, 2, 3), 4, 8, 0), ((100,), 4, 200, 1), ((0, 0), 4, 3, 0)])
+def test_balanced_row_split(lib, seqlens, kpool, parts, row_weight):
+    cu = np.cumsum([0] + list(seqlens)).astype(np.int32)
+    b = K.kpool_balanced_row_split(cu, kpool, parts, row_weight)
+    T = int(cu[-1])
+    assert len(b) == parts + 1 and b[0] == 0 and b[-1] == T
+    assert all(x <= y for x, y in zip(b, b[1:]))
+    work = _pairs_per_row(cu, kpool) + row_weight
+    prefix = np.concatenate([[0], np.cumsum(work)])
+    total = int(prefix[-1])
+    for g in range(1, parts):
+        # boundary g is the first row whose preceding work reaches g/parts of the total
+        target = (total // parts) * g + ((total % parts) * g) // parts
+        assert prefix[b[g]] >= target
+        assert b[g] == 0 or prefix[b[g] - 1] < target
+    # so every range's work is within one row's work of an equal share
+    share, row_max = total / parts, int(work.max()) if len(work) else 0
+    for g in range(parts):
+        assert abs(int(prefix[b[g + 1]] - prefix[b[g]]) - share) <= row_max + 1
+
+
+def test_balanced_row_split_validation(lib):
+    P = ctypes.c_void_p
+    cu = np.array([0, 10, 5], dtype=np.int32)
+    out = np.zeros(4, dtype=np.int32)
+    ptr = lambda a: a.ctypes.data_as(P)  # noqa: E731
+    assert lib.kpool_balanced_row_split(ptr(cu), 2, 4, 0, 3, ptr(out)) == K.KPOOL_ERR_INVALID_ARG  # decreasing
+    cu = np.array([0, 10], dtype=np.int32)
+    assert lib.kpool_balanced_row_split(ptr(cu), 1, 0, 0, 3, ptr(out)) == K.KPOOL_ERR_INVALID_ARG  # kpool
+    assert lib.kpool_balanced_row_split(ptr(cu), 1, 4, 0, 0, ptr(out)) == K.KPOOL_ERR_INVALID_ARG  # parts
+    assert lib.kpool_balanced_row_split(ptr(cu), 1, 4, -1, 3, ptr(out)) == K.KPOOL_ERR_INVALID_ARG
+    assert lib.kpool_balanced_row_split(None, 1, 4, 0, 3, ptr(out)) == K.KPOOL_ERR_INVALID_ARG
