@@ -263,8 +263,9 @@ kpool_status kpool_pool_keys(const void* k, const int32_t* cu_seqlens, int32_t n
   int sms = 0;
   if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, 0, total_tokens, ws, L, stream)))
-    return KPOOL_ERR_CUDA;
+  // pooling needs the checked bounds and the pool offsets only: an empty row range
+  // leaves the work list empty
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, 0, 0, ws, L, stream))) return KPOOL_ERR_CUDA;
   if (!cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool, out_pooled_keys, ws, L,
                            sms, stream)))
     return KPOOL_ERR_CUDA;
@@ -290,8 +291,7 @@ kpool_status kpool_pool_keys_gated(const void* k, const float* gate, const float
   int sms = 0;
   if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, 0, total_tokens, ws, L, stream)))
-    return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, total_tokens, kpool, 0, 0, ws, L, stream))) return KPOOL_ERR_CUDA;
   if (!cuda_ok(launch_pool_gated(k, gate, ape, dtype, cu_seqlens, num_seqs, total_tokens, head_dim, kpool,
                                  out_pooled_keys, ws, L, sms, stream)))
     return KPOOL_ERR_CUDA;

@@ -8,8 +8,9 @@
 // nearest even in the input dtype -- so a bf16 MMA consumes it exactly.
 //
 // HBM-bound: each thread owns one 16-byte chunk (8 bf16 / 4 fp32 channels) of
-// one pooled row, reads kpool 16-byte vectors (coalesced across the chunk
-// threads of a row) and writes one. Grid-stride over P * d/vec chunks.
+// one pooled row at a time, reads kpool 16-byte vectors (coalesced across the
+// chunk threads of a row) and writes one. Grid-stride over P * d/vec chunks;
+// kpool = 4 has its own kernels that keep more loads in flight.
 #include <cuda_bf16.h>
 
 #include "kpool_internal.cuh"
@@ -87,6 +88,72 @@ __global__ void __launch_bounds__(256) pool_kernel(const T* __restrict__ k, cons
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = __fdiv_rn(acc[e], divisor);
     *reinterpret_cast<uint4*>(out + g * d + c) = pack(acc, static_cast<T*>(nullptr));
+  }
+}
+
+// Sequence of global pool row g: last b with pool_off[b] <= g.
+__device__ __forceinline__ int seq_of_pool(const int32_t* __restrict__ pool_off, int S, int64_t g) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (int64_t(__ldg(pool_off + mid)) <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// pool_kernel for a compile-time kpool (the pages' kpool is 4): each thread takes
+// kUnroll chunks per round and issues all kUnroll * KP 16-byte loads before any add,
+// so a warp keeps kUnroll * KP independent loads in flight instead of one per
+// dependent add. The keys are read once (evict-first loads); the pooled keys are
+// written with the default policy so the score kernel that follows finds them in L2.
+// Dividing by KP = 4 is an exact power-of-two scaling, so multiplying by 1/KP rounds
+// to the same value as the IEEE division of the generic kernel.
+template <typename T, int KP>
+__global__ void __launch_bounds__(256) pool_kernel_fixed(const T* __restrict__ k, const int32_t* __restrict__ cu,
+                                                         const int32_t* __restrict__ pool_off,
+                                                         const WorkspaceHeader* __restrict__ hdr, int S, int d,
+                                                         T* __restrict__ out) {
+  constexpr int V = Vec<T>::kLanes;
+  constexpr int kUnroll = 2;
+  static_assert((KP & (KP - 1)) == 0, "1/KP must be exact");
+  if (hdr->error != 0) return;
+  const int64_t P = hdr->total_pools;
+  const int chunks = d / V;
+  const int64_t total = P * chunks;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i0 = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i0 < total; i0 += kUnroll * stride) {
+    uint4 v[kUnroll][KP];
+    int64_t dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = i0 + u * stride;
+      dst[u] = -1;
+      if (i < total) {
+        const int64_t g = i / chunks;  // global pool row
+        const int c = int(i - g * chunks) * V;
+        const int b = seq_of_pool(pool_off, S, g);
+        const int64_t first = int64_t(__ldg(cu + b)) + (g - __ldg(pool_off + b)) * KP;
+        const uint4* src = reinterpret_cast<const uint4*>(k + first * d + c);
+#pragma unroll
+        for (int j = 0; j < KP; ++j) v[u][j] = __ldcs(src + j * (d / V));
+        dst[u] = g * d + c;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (dst[u] < 0) continue;
+      float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int j = 0; j < KP; ++j) {
+        float f[8];
+        unpack(v[u][j], f, static_cast<T*>(nullptr));
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = __fmul_rn(acc[e], 1.0f / KP);
+      *reinterpret_cast<uint4*>(out + dst[u]) = pack(acc, static_cast<T*>(nullptr));
+    }
   }
 }
 
@@ -194,6 +261,76 @@ __global__ void __launch_bounds__(256) pool_gated_kernel(const T* __restrict__ k
   }
 }
 
+// pool_gated_kernel for a compile-time kpool: every load of a chunk (KP keys, KP
+// rows of gate scores, the embedding) is issued before the arithmetic, which is the
+// generic kernel's, term for term and in the same order.
+template <typename T, int KP>
+__global__ void __launch_bounds__(256) pool_gated_kernel_fixed(const T* __restrict__ k,
+                                                               const float* __restrict__ gate,
+                                                               const float* __restrict__ ape,
+                                                               const int32_t* __restrict__ cu,
+                                                               const int32_t* __restrict__ pool_off,
+                                                               const WorkspaceHeader* __restrict__ hdr, int S, int d,
+                                                               T* __restrict__ out) {
+  constexpr int V = Vec<T>::kLanes;
+  if (hdr->error != 0) return;
+  const int64_t P = hdr->total_pools;
+  const int chunks = d / V;
+  const int64_t total = P * chunks;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t g = i / chunks;  // global pool row
+    const int c = int(i - g * chunks) * V;
+    const int b = seq_of_pool(pool_off, S, g);
+    const int64_t first = int64_t(__ldg(cu + b)) + (g - __ldg(pool_off + b)) * KP;
+    uint4 kv[KP];
+    float4 gv4[KP][V / 4];
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+      kv[j] = __ldcs(reinterpret_cast<const uint4*>(k + (first + j) * d + c));
+#pragma unroll
+      for (int h = 0; h < V / 4; ++h) gv4[j][h] = __ldcs(reinterpret_cast<const float4*>(gate + (first + j) * d + c) + h);
+    }
+    float m[8], den[8], num[8];
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      m[e] = -INFINITY;
+      den[e] = 0.0f;
+      num[e] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+      const float* gv = reinterpret_cast<const float*>(&gv4[j][0]);
+#pragma unroll
+      for (int e = 0; e < V; ++e) m[e] = fmaxf(m[e], gv[e]);
+    }
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+      float f[8];
+      unpack(kv[j], f, static_cast<T*>(nullptr));
+      const float* gv = reinterpret_cast<const float*>(&gv4[j][0]);
+      const float4* ap = reinterpret_cast<const float4*>(ape + int64_t(j) * d + c);
+      float av[8];
+#pragma unroll
+      for (int h = 0; h < V / 4; ++h) {
+        const float4 x = __ldg(ap + h);
+        av[4 * h] = x.x;
+        av[4 * h + 1] = x.y;
+        av[4 * h + 2] = x.z;
+        av[4 * h + 3] = x.w;
+      }
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const float ge = expf(gv[e] - m[e]);
+        den[e] = __fadd_rn(den[e], ge);
+        num[e] = __fadd_rn(num[e], __fmul_rn(ge, __fadd_rn(f[e], av[e])));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) num[e] = __fdiv_rn(num[e], den[e]);
+    *reinterpret_cast<uint4*>(out + g * d + c) = pack(num, static_cast<T*>(nullptr));
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_pool_gated(const void* k, const float* gate, const float* ape, kpool_dtype dtype,
@@ -207,7 +344,15 @@ cudaError_t launch_pool_gated(const void* k, const float* gate, const float* ape
   if (blocks > cap) blocks = cap;
   const auto* hdr = reinterpret_cast<const WorkspaceHeader*>(ws + L.header);
   const auto* pool_off = reinterpret_cast<const int32_t*>(ws + L.pool_off);
-  if (dtype == KPOOL_BF16)
+  if (kpool == 4) {
+    if (dtype == KPOOL_BF16)
+      pool_gated_kernel_fixed<__nv_bfloat16, 4><<<unsigned(blocks), threads, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(k), gate, ape, cu, pool_off, hdr, S, d,
+          static_cast<__nv_bfloat16*>(out));
+    else
+      pool_gated_kernel_fixed<float, 4><<<unsigned(blocks), threads, 0, stream>>>(
+          static_cast<const float*>(k), gate, ape, cu, pool_off, hdr, S, d, static_cast<float*>(out));
+  } else if (dtype == KPOOL_BF16)
     pool_gated_kernel<__nv_bfloat16><<<unsigned(blocks), threads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(k), gate, ape, cu, pool_off, hdr, S, d, kpool,
         static_cast<__nv_bfloat16*>(out));
@@ -229,7 +374,17 @@ cudaError_t launch_pool(const void* k, kpool_dtype dtype, const int32_t* cu, int
   if (blocks > cap) blocks = cap;
   const auto* hdr = reinterpret_cast<const WorkspaceHeader*>(ws + L.header);
   const auto* pool_off = reinterpret_cast<const int32_t*>(ws + L.pool_off);
-  if (dtype == KPOOL_BF16)
+  if (kpool == 4) {
+    // one wave: the fixed kernel's registers allow 4 CTAs of 256 threads per SM
+    if (blocks > int64_t(num_sms) * 4) blocks = int64_t(num_sms) * 4;
+    if (dtype == KPOOL_BF16)
+      pool_kernel_fixed<__nv_bfloat16, 4><<<unsigned(blocks), threads, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(k), cu, pool_off, hdr, S, d, static_cast<__nv_bfloat16*>(out));
+    else
+      pool_kernel_fixed<float, 4><<<unsigned(blocks), threads, 0, stream>>>(static_cast<const float*>(k), cu,
+                                                                           pool_off, hdr, S, d,
+                                                                           static_cast<float*>(out));
+  } else if (dtype == KPOOL_BF16)
     pool_kernel<__nv_bfloat16><<<unsigned(blocks), threads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(k), cu, pool_off, hdr, S, d, kpool, static_cast<__nv_bfloat16*>(out));
   else
