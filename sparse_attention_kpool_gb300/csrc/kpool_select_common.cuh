@@ -28,110 +28,6 @@ __device__ inline void warp_sort_desc(uint64_t* buf, int n) {
   }
 }
 
-// Threshold search + compaction, one warp, n <= 32 * kSlots keys.
-//
-// Finds an edge such that budget <= #{keys >= edge} <= budget + slack by a
-// most-significant-digit search with 5-bit digits: each pass histograms the
-// keys of the current bin on the five bits just below their highest differing
-// bit (so common leading bits cost nothing) and descends into the bin where the
-// running count crosses `budget`, until the whole bin can be kept. Keys are
-// distinct, so every pass splits the bin and the search ends. The kept keys are
-// then written back to the front of buf (unordered). Requires budget <= n.
-// `hist` is 16 words of shared memory private to the warp holding 32 16-bit
-// bin counts (n < 65536). Returns the kept count; *edge_out receives the edge
-// (keys below it cannot be in the top budget).
-template <int kSlots>
-__device__ inline int warp_select_compact(uint64_t* buf, int n, int budget, int slack, uint32_t* hist,
-                                          uint64_t* edge_out) {
-  const int lane = threadIdx.x & 31;
-  const unsigned full = 0xffffffffu;
-  uint64_t key[kSlots];
-#pragma unroll
-  for (int i = 0; i < kSlots; ++i) {
-    const int idx = i * 32 + lane;
-    key[i] = idx < n ? buf[idx] : 0ull;
-  }
-  __syncwarp();
-
-  bool all = true;   // the current bin is every nonzero key
-  int bin_shift = 0; // otherwise: keys with (key >> bin_shift) == bin_hi
-  uint64_t bin_hi = 0;
-  int above = 0;     // keys above the current bin (all kept)
-  uint64_t edge = 1;
-  for (int pass = 0; pass < 64; ++pass) {
-    // common bits of the bin's keys
-    uint64_t o = 0, a = ~0ull;
-#pragma unroll
-    for (int i = 0; i < kSlots; ++i) {
-      const bool in = key[i] != 0 && (all || (key[i] >> bin_shift) == bin_hi);
-      if (in) {
-        o |= key[i];
-        a &= key[i];
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      o |= __shfl_xor_sync(full, o, off);
-      a &= __shfl_xor_sync(full, a, off);
-    }
-    const uint64_t diff = o ^ a;
-    if (diff == 0) {  // one key left in the bin: it completes the budget
-      edge = a;
-      break;
-    }
-    const int top = 63 - __clzll(static_cast<long long>(diff));
-    const int dshift = top >= 4 ? top - 4 : 0;
-    if (lane < 16) hist[lane] = 0;
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < kSlots; ++i) {
-      const bool in = key[i] != 0 && (all || (key[i] >> bin_shift) == bin_hi);
-      if (in) {
-        const uint32_t digit = uint32_t(key[i] >> dshift) & 31u;
-        atomicAdd(hist + (digit >> 1), 1u << (16 * (digit & 1u)));
-      }
-    }
-    __syncwarp();
-    const int cnt = int((hist[lane >> 1] >> (16 * (lane & 1))) & 0xFFFFu);
-    int suffix = cnt;  // sum of counts of digits >= lane
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_down_sync(full, suffix, off);
-      if (lane + off < 32) suffix += v;
-    }
-    const int higher = suffix - cnt;  // digits > lane
-    const unsigned hit = __ballot_sync(full, above + higher < budget && above + suffix >= budget);
-    const int d = __ffs(hit) - 1;
-    const int d_higher = __shfl_sync(full, higher, d);
-    const int d_cnt = __shfl_sync(full, cnt, d);
-    __syncwarp();
-    // bits above the digit are common to the whole bin (taken from the AND)
-    const uint64_t upper = (dshift + 5 >= 64) ? 0ull : ((a >> (dshift + 5)) << 5);
-    const uint64_t new_hi = upper | uint64_t(d);
-    if (above + d_higher + d_cnt <= budget + slack || dshift == 0) {
-      edge = new_hi << dshift;
-      break;
-    }
-    above += d_higher;
-    all = false;
-    bin_shift = dshift;
-    bin_hi = new_hi;
-  }
-
-  // write the kept keys back to the front of buf
-  int base = 0;
-#pragma unroll
-  for (int i = 0; i < kSlots; ++i) {
-    const bool keep = key[i] != 0 && key[i] >= edge;
-    const unsigned m = __ballot_sync(full, keep);
-    if (keep) buf[base + __popc(m & ((1u << lane) - 1u))] = key[i];
-    base += __popc(m);
-  }
-  __syncwarp();
-  *edge_out = edge;
-  return base;
-}
-
 // Compare-exchange of a bitonic network on 64-bit keys: returns the key this
 // position keeps, the larger of (mine, other) when keep_max, else the smaller.
 __device__ __forceinline__ uint64_t bitonic_keep(uint64_t mine, uint64_t other, bool keep_max) {

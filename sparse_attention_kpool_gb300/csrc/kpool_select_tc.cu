@@ -36,8 +36,11 @@
 //               warp w reads TMEM lanes 32*(w%4).. (the hardware rule). The
 //               groups synchronise only within themselves. Per row: tcgen05.ld
 //               (the next row's columns and head weights load meanwhile) -> relu,
-//               |scale|*w, head sum in fp32 (packed f32x2 FMAs) -> selection key
-//               -> threshold filter -> candidate buffer in shared memory.
+//               |scale|*w, head sum in fp32 -> selection key -> threshold filter
+//               -> candidate buffer in shared memory. The relu runs on the FMA
+//               pipe as x + |x| (twice relu(x), exactly) against halved weights,
+//               so packed f32x2 FMAs round the same products as w * relu(x) while
+//               the ALU pipe carries only the selection's integer work.
 // Selection: 1536 candidate slots per query row, in four 384-slot regions, one
 // per warp of the owning group, so a warp appends with a register count and no
 // atomics. A key enters only if it beats the row's threshold. When a region
@@ -494,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rbase = 4 * grp;        // the group's first row
     const int bar_id = 1 + grp;
     SelectScratch* sel = reinterpret_cast<SelectScratch*>(smem + kOffSelect + grp * kSelectBytes);
+    uint64_t* const my_region = s_cand + rbase * kCap + wq * kReg;  // this warp's region of the group's row 0
     const unsigned lt_mask = (1u << lane) - 1u;
     const uint32_t lane_addr = tmem_base + (uint32_t(lg * 32) << 16);
     int acc = 0;
@@ -523,7 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int q = rbase + (gt >> 5), h = gt & 31;
         const int row = it.t0 + q;
-        s_w[q * kHeads + h] = row < it.len ? w[(it.seq_start + row) * kHeads + h] * abs_scale : 0.0f;
+        // halved: the scoring loop multiplies by x + |x| = 2 relu(x) (exact)
+        s_w[q * kHeads + h] = row < it.len ? (w[(it.seq_start + row) * kHeads + h] * abs_scale) * 0.5f : 0.0f;
       }
       if (gt < 4) {
         const int q = rbase + gt;
@@ -534,11 +539,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cnt[4] = {0, 0, 0, 0};  // this warp's region counts of the group's four rows
       named_bar(bar_id, 128);
       bool aborted = false;
+      bool overflow = false;  // a region passed its capacity (a library bug; see the insertion)
       for (int i = 0; i < it.n_tiles; ++i) {
-        bool ready = true;
         bool over = false;  // this warp's reservation pushed a row past the compaction mark
-        if (lane == 0) ready = ptx::mbar_wait_bounded(bar.acc_full + acc, acc_phase, kMaxPolls, kMaxWaitNs);
-        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+        // every lane tests the barrier (one warp-wide instruction, no divergent branch);
+        // the vote keeps a wait that ran out uniform across the warp
+        const bool ready = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(bar.acc_full + acc, acc_phase, kMaxPolls,
+                                                                          kMaxWaitNs));
         if (!ready) {
           record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
           *abort_flag = 1;
@@ -552,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ulonglong2 wr[2][kHeads / 4];
           uint64_t key[4];
           unsigned m[4];
+          bool pass[4];
           ptx::tc_ld_32x32b_x32(col0, v[0]);
           {
             const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(s_w + rbase * kHeads);
@@ -584,33 +592,39 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float x1 = __uint_as_float(cur[4 * h4 + 1]);
               const float x2 = __uint_as_float(cur[4 * h4 + 2]);
               const float x3 = __uint_as_float(cur[4 * h4 + 3]);
-              acc0 = ptx::fma_f32x2(ww.x, ptx::pack_f32x2(fmaxf(kNegScale ? -x0 : x0, 0.0f),
-                                                          fmaxf(kNegScale ? -x1 : x1, 0.0f)), acc0);
-              acc1 = ptx::fma_f32x2(ww.y, ptx::pack_f32x2(fmaxf(kNegScale ? -x2 : x2, 0.0f),
-                                                          fmaxf(kNegScale ? -x3 : x3, 0.0f)), acc1);
+              // relu on the FMA pipe: x + |x| is exactly 2 relu(x) (|x| - x for a negative
+              // scale; the absolute value is an operand modifier of the add), and the weights
+              // are halved, so each fused multiply-add rounds the same exact product as
+              // w * relu(x) would; the ALU pipe is left to the selection
+              acc0 = ptx::fma_f32x2(ww.x, ptx::pack_f32x2(kNegScale ? fabsf(x0) - x0 : x0 + fabsf(x0),
+                                                          kNegScale ? fabsf(x1) - x1 : x1 + fabsf(x1)), acc0);
+              acc1 = ptx::fma_f32x2(ww.y, ptx::pack_f32x2(kNegScale ? fabsf(x2) - x2 : x2 + fabsf(x2),
+                                                          kNegScale ? fabsf(x3) - x3 : x3 + fabsf(x3)), acc1);
             }
             float s0, s1, s2, s3;
             ptx::unpack_f32x2(acc0, s0, s1);
             ptx::unpack_f32x2(acc1, s2, s3);
             const float s = (s0 + s1) + (s2 + s3);
             key[j] = make_key(s, uint32_t(p));
-            m[j] = __ballot_sync(0xffffffffu, p < s_elig[q] && key[j] > s_tau[q]);
+            pass[j] = p < s_elig[q] && key[j] > s_tau[q];
+            m[j] = __ballot_sync(0xffffffffu, pass[j]);
             if (j < 3) {
               ptx::tc_wait_ld();
               ptx::tc_reg_fence(v[(j + 1) & 1]);
             }
           }
           // append to this warp's region of each row (warp-uniform counts, no atomics)
+          // A region holds at most kRegMark keys when a tile starts (a compaction runs as
+          // soon as one passes the mark) and a tile adds at most 32, so every slot below
+          // is < kReg without a per-key check.
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int slot = cnt[j] + __popc(m[j] & lt_mask);
-            if (((m[j] >> lane) & 1u) && slot < kReg) s_cand[(rbase + j) * kCap + wq * kReg + slot] = key[j];
+            if (pass[j]) my_region[j * kCap + cnt[j] + __popc(m[j] & lt_mask)] = key[j];
             cnt[j] += __popc(m[j]);
-            over = over || cnt[j] > kRegMark;
           }
-          // cannot happen (kRegMark leaves room for a tile); the stores above skip it
-          if (lane == 0 && (cnt[0] > kReg || cnt[1] > kReg || cnt[2] > kReg || cnt[3] > kReg))
-            record_error(hdr, KPOOL_ERR_INTERNAL);
+          const int cmax = max(max(cnt[0], cnt[1]), max(cnt[2], cnt[3]));
+          over = cmax > kRegMark;
+          overflow = overflow || cmax > kReg;  // cannot happen; reported at the end of the item
         }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
@@ -637,6 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (aborted) break;
+      if (overflow && lane == 0) record_error(hdr, KPOOL_ERR_INTERNAL);
       // final ranking: cut each of the group's rows to its top `budget` keys, dealt
       // evenly over the four regions (the group's four warps together), then warp wq
       // sorts row rbase + wq and writes it
