@@ -52,10 +52,10 @@ PAGES_SEC_512K = 21.07
 # DRAM traffic of the score+select kernel from one ncu capture, per launch at the
 # pages-scale workload, tied to the kernel source it was measured on: when the
 # source hash differs the number is stale and is reported as null.
-NCU_TRAFFIC = {"kernel_sha256": "dddbed140292a189", "workload": "pages_512k",
-               # long_128k capture: 1.103 GB read + 0.214 GB written per launch; q, w and the
+NCU_TRAFFIC = {"kernel_sha256": "7d538d9c030732b9", "workload": "pages_512k",
+               # long_128k capture: 1.102391 GB read + 0.213307 GB written per launch; q, w and the
                # pool ids grow with the rows, so x4 at 524288 tokens
-               "bytes_per_launch": 4 * (1.103136e9 + 0.213674e9)}
+               "bytes_per_launch": 4 * (1.102391296e9 + 0.21330688e9)}
 
 
 def source_sha(path: str) -> str:
@@ -264,8 +264,9 @@ def rows_config(wl: W.RowsWorkload, world: int) -> dict:
 ROWS_METRIC = "KPool decode selection: scored pairs/s (rows against a pooled-key cache)"
 
 
-def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
-    """Decode / short-query path: kpool_select_rows against a resident pooled-key cache."""
+def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int, emit: bool = True):
+    """Decode / short-query path: kpool_select_rows against a resident pooled-key cache.
+    Prints the JSON line on rank 0 when `emit`, and returns it."""
     if args.impl == "reference":
         if rank == 0:
             from oracle import oracle
@@ -453,8 +454,9 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int):
             ok = False
             line["parity_sample_error"] = str(ex)[:200]
         line["parity_sample"] = {"rows": R, "ok": ok}
-    if rank == 0:
+    if rank == 0 and emit:
         print(json.dumps(line), flush=True)
+    return line
 
 
 def main():
@@ -469,6 +471,8 @@ def main():
     ap.add_argument("--ref-pairs-per-step", type=float, default=1.5e7)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode workload that the default (pages-scale) run also measures")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -564,9 +568,11 @@ def main():
 
     # ---- end to end through the C ABI with host buffers: every step copies its inputs
     # from pinned host memory and its pool and token ids back, pipelined the way a caller
-    # would drive the library -- two device buffer sets, the next step's inputs upload on
-    # one copy stream and the previous step's results download on another while the
-    # current step computes on the main stream
+    # would drive the library -- two device buffer sets; while step i computes on the main
+    # stream, one copy stream downloads step i-1's results and then uploads step i+1's
+    # inputs. Uploads and downloads share that stream on purpose: on this host, a download
+    # running at the same time as an upload slows both several-fold, while one after the
+    # other they take ~50 ms of a ~220 ms step.
     e2e = None
     if not args.no_e2e:
         h_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
@@ -579,51 +585,104 @@ def main():
         h_toks = [torch.empty(toks.shape, dtype=toks.dtype, pin_memory=True) for _ in range(2)]
         bi = sum(v.numel() * v.element_size() for v in h_in.values())
         bo = h_ids[0].numel() * 4 + h_toks[0].numel() * 4
-        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        up = torch.cuda.Stream()
+        down = up  # one copy stream (see above)
         computed = [torch.cuda.Event(), torch.cuda.Event()]
         uploaded = [torch.cuda.Event(), torch.cuda.Event()]
         downloaded = [torch.cuda.Event(), torch.cuda.Event()]
+        # timeline of the timed steps: upload, selection and download intervals on their own
+        # streams (events on the stream each interval runs on)
+        tl = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
 
-        def e2e_steps(n):
+        def e2e_steps(n, marks=None):
+            def download(j):
+                b = j & 1
+                ev = marks[j] if marks is not None else None
+                up.wait_event(computed[b])
+                with torch.cuda.stream(up):
+                    if ev:
+                        ev[4].record(up)
+                    h_ids[b].copy_(d_ids[b], non_blocking=True)
+                    h_toks[b].copy_(d_toks[b], non_blocking=True)
+                    downloaded[b].record(up)
+                    if ev:
+                        ev[5].record(up)
+
             for i in range(n):
                 b = i & 1
-                if i >= 2:
-                    up.wait_event(computed[b])        # step i-2 is done reading these inputs
+                ev = marks[i] if marks is not None else None
+                # step i's inputs go into the buffers step i-2 read: the copy stream passed
+                # step i-2's `computed` event before downloading its results
                 with torch.cuda.stream(up):
+                    if ev:
+                        ev[0].record(up)
                     for k in h_in:
                         d_in[b][k].copy_(h_in[k], non_blocking=True)
                     uploaded[b].record(up)
+                    if ev:
+                        ev[1].record(up)
                 stream.wait_event(uploaded[b])
                 if i >= 2:
                     stream.wait_event(downloaded[b])  # step i-2's results have left these buffers
+                if ev:
+                    ev[2].record(stream)
                 K.kpool_select_ex(d_in[b]["q"], d_in[b]["k"], d_in[b]["w"], d_in[b]["cu_seqlens"], wl.kpool,
                                   wl.index_topk, wl.scale, out_pool_ids=d_ids[b], out_token_ids=d_toks[b],
                                   workspace=ws, stream=stream)
                 computed[b].record(stream)
-                down.wait_event(computed[b])
-                with torch.cuda.stream(down):
-                    h_ids[b].copy_(d_ids[b], non_blocking=True)
-                    h_toks[b].copy_(d_toks[b], non_blocking=True)
-                    downloaded[b].record(down)
+                if ev:
+                    ev[3].record(stream)
+                if i >= 1:
+                    download(i - 1)  # runs while step i computes
+            download(n - 1)
 
         e2e_steps(2)
         torch.cuda.synchronize()
+        # the same upload alone (nothing else on the GPU), to tell copy speed from overlap effects
+        iso = []
+        for _ in range(2):
+            a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(up):
+                a0.record(up)
+                for k in h_in:
+                    d_in[1][k].copy_(h_in[k], non_blocking=True)
+                b0.record(up)
+            torch.cuda.synchronize()
+            iso.append(a0.elapsed_time(b0))
         barrier(world)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         up.wait_stream(stream)
-        down.wait_stream(stream)
-        e2e_steps(args.steps)
+        e2e_steps(args.steps, tl)
         stream.wait_stream(up)
-        stream.wait_stream(down)
         b.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, world)
+        med = lambda xs: statistics.median(xs) if xs else None  # noqa: E731
+        timeline = {
+            "upload_ms": med([e[0].elapsed_time(e[1]) for e in tl]),
+            "select_ms": med([e[2].elapsed_time(e[3]) for e in tl]),
+            "download_ms": med([e[4].elapsed_time(e[5]) for e in tl]),
+            # time the selection stream sat idle between two selections (waiting on copies)
+            "select_gap_ms": med([tl[i - 1][3].elapsed_time(tl[i][2]) for i in range(1, len(tl))]),
+            "select_gap_total_ms": sum(tl[i - 1][3].elapsed_time(tl[i][2]) for i in range(1, len(tl))),
+            "upload_max_ms": max(e[0].elapsed_time(e[1]) for e in tl),
+            "upload_ms_by_step": [round(e[0].elapsed_time(e[1]), 2) for e in tl],
+            "download_ms_by_step": [round(e[4].elapsed_time(e[5]), 2) for e in tl],
+            "download_max_ms": max(e[4].elapsed_time(e[5]) for e in tl),
+            "exposed_first_upload_ms": a.elapsed_time(tl[0][2]),
+            "exposed_last_download_ms": tl[-1][3].elapsed_time(b),
+            "select_alone_ms": ms_step,
+            "upload_alone_ms": min(iso),
+            "note": "medians over the timed steps; select_ms against select_alone_ms shows whether the selection "
+                    "slows while copies run, select_gap_ms whether it waits on them"}
         e2e = {"value": world * pairs / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
-               "pipelining": "2 buffer sets; uploads and downloads on two copy streams overlap compute"}
+               "pipelining": "2 buffer sets; one copy stream downloads step i-1 and uploads step i+1 while step i "
+                             "computes",
+               "timeline": timeline}
         st = K.kpool_last_device_error(ws)
         if st != K.KPOOL_OK:
             raise K.KpoolError(st, "device (end-to-end run)")
@@ -682,6 +741,16 @@ def main():
             "work": "full query x pool rectangle (2x the causal pairs counted here)",
             "ratio_of_seconds": PAGES_SEC_512K / (ms_step / 1e3)}
 
+    if wl.name == "pages_512k" and not args.no_decode:
+        # the decode workload (16 rows against 262,144-token key caches) measured in the same
+        # run, so its numbers come with the default bench line; its own oracle timing and
+        # parity sample run only in its standalone run (--workload decode_262k)
+        dec_args = argparse.Namespace(**vars(args))
+        dec_args.steps, dec_args.warmup, dec_args.no_cpu = max(args.steps, 20), max(args.warmup, 5), True
+        dec = rows_bench(dec_args, W.DECODE_262K, world, rank, emit=False)
+        line["decode_262k"] = {k: dec[k] for k in ("metric", "value", "unit", "ms_per_step", "us_per_decode_step",
+                                                   "us_per_decode_step_graph", "kernel_ms", "roofline", "clocks",
+                                                   "config", "e2e", "steps", "warmup")}
     if rank == 0 and not args.no_cpu:
         rows = pick_sample_rows(wl, args.cpu_sample_pairs, seed=7)
         res = oracle_sample(inp, wl, rows)
