@@ -566,6 +566,22 @@ def main():
     gated_ms = ga.elapsed_time(gb) / args.steps  # plan + gated pooling
     del gate, kp_g, gws
 
+    # a device-to-device copy moving the same number of bytes as the mean pooling (half read,
+    # half written): what a transfer of this size reaches on this GPU, for context
+    half = (T * d * 2 + wl.num_pools() * d * 2) // 2
+    c_src = torch.empty(half, dtype=torch.uint8, device=dev)
+    c_dst = torch.empty_like(c_src)
+    c_ts = []
+    for _ in range(args.warmup + 10):
+        ca, cb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ca.record(stream)
+        c_dst.copy_(c_src)
+        cb.record(stream)
+        torch.cuda.synchronize()
+        c_ts.append(ca.elapsed_time(cb))
+    copy_same_ms = statistics.median(c_ts[args.warmup:])
+    del c_src, c_dst
+
     # ---- end to end through the C ABI with host buffers: every step copies its inputs
     # from pinned host memory and its pool and token ids back, pipelined the way a caller
     # would drive the library -- two device buffer sets; while step i computes on the main
@@ -723,7 +739,8 @@ def main():
                      "algorithmic_bytes_per_launch": k2_bytes},
         "hbm_kernels": {
             "pool": {"bytes": k1_bytes, "GB/s": k1_bytes / (k_ms[1] / 1e3) / 1e9,
-                     "frac": k1_bytes / (k_ms[1] / 1e3) / 1e9 / hbm},
+                     "frac": k1_bytes / (k_ms[1] / 1e3) / 1e9 / hbm,
+                     "same_size_copy_GB/s": 2 * half / (copy_same_ms / 1e3) / 1e9},
             "expand": {"bytes": k3_bytes, "GB/s": k3_bytes / (k_ms[3] / 1e3) / 1e9,
                        "frac": k3_bytes / (k_ms[3] / 1e3) / 1e9 / hbm},
             "pool_gated": {"bytes": kg_bytes, "ms": gated_ms, "GB/s": kg_bytes / (gated_ms / 1e3) / 1e9,
@@ -772,6 +789,17 @@ def main():
             ok = False
             line["parity_sample_error"] = str(ex)[:200]
         line["parity_sample"] = {"rows": int(len(rows)), "ok": ok}
+        if wl.values == "integer":
+            # rows of the sample where an exact tie straddles the budget cutoff (rank budget and
+            # rank budget + 1 score the same, so the smaller-index rule decides): a one-slot-wider
+            # oracle selection of the same rows
+            from oracle import oracle as orc
+            cu_h = inp["cu_seqlens"].cpu().numpy()
+            wide = orc.select(parity.bits(inp["q"][r]), inp["w"][r].cpu().numpy(), res["kp"], cu_h, rows, wl.dtype,
+                              wl.kpool, wl.index_topk + wl.kpool, wl.scale)
+            line["cutoff_tie_rows"] = {"rows": int(len(parity.cutoff_tie_rows(wide, wl.budget))),
+                                       "of_sampled": int(len(rows)),
+                                       "with_more_eligible_than_budget": int((wide["eligible"] > wl.budget).sum())}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
