@@ -56,6 +56,9 @@ NCU_TRAFFIC = {"kernel_sha256": "7d538d9c030732b9", "workload": "pages_512k",
                # long_128k capture: 1.102391 GB read + 0.213307 GB written per launch; q, w and the
                # pool ids grow with the rows, so x4 at 524288 tokens
                "bytes_per_launch": 4 * (1.102391296e9 + 0.21330688e9)}
+# The same for the index-score mode of that kernel, per launch of the long_128k chunked run
+# (the mean over one step's chunk launches); None until captured.
+NCU_TRAFFIC_SCORES = {"kernel_sha256": None, "workload": "long_128k", "bytes_per_launch": None}
 
 
 def source_sha(path: str) -> str:
@@ -459,6 +462,195 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int, emit: bool = Tru
     return line
 
 
+SCORES_METRIC = "KPool index scores: scored pairs/s (full masked [rows, pools] fp32 scores, row chunks <= 2 GiB)"
+# The pages compute their index scores in row chunks of at most 2 GiB (NVIDIA/Megatron-LM
+# pull request #8299, "Change"); the benchmark chunks the same way.
+SCORE_CHUNK_BYTES = 2 << 30
+
+
+def scores_config(wl: W.Workload, world: int, ld: int, chunk: int, nck: int) -> dict:
+    c = workload_config(wl, world)
+    c.update({"ld": ld, "chunk_rows": chunk, "chunks": nck,
+              "output": "fp32 [rows, ld] per chunk into one reused device buffer",
+              "l2": "inputs larger than L2 (q %.1f GiB, each chunk's output %.1f GiB)" % (
+                  wl.total_tokens * wl.heads * wl.head_dim * 2 / 2**30, chunk * ld * 4 / 2**30)})
+    c.pop("index_topk")
+    c.pop("budget")
+    return c
+
+
+def index_scores_bench(args, wl: W.Workload, world: int, rank: int, emit: bool = True):
+    """Full index scores of every row (kpool_pool_keys once, then kpool_index_scores_pooled
+    per row chunk of <= 2 GiB of output). Prints the JSON line on rank 0 when `emit`, and
+    returns it."""
+    kbuild.build()
+    K.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    inp = W.generate(wl, dev)
+    T, H, d = wl.total_tokens, wl.heads, wl.head_dim
+    ld = max(1, max(int(L) // wl.kpool for L in wl.seqlens))  # the widest row any sequence has
+    chunk = max(1, min(T, SCORE_CHUNK_BYTES // (4 * ld)))
+    bounds = list(range(0, T, chunk)) + [T]
+    nck = len(bounds) - 1
+    dt_code = K.KPOOL_BF16 if wl.dtype == "bf16" else K.KPOOL_F32
+    ws = K.new_workspace(T, wl.num_seqs, H, d, dt_code, wl.kpool, 0, dev)
+    out = [torch.empty((chunk, ld), dtype=torch.float32, device=dev) for _ in range(2)]
+    kp = torch.empty((max(1, T // wl.kpool), d), dtype=inp["k"].dtype, device=dev)
+    pairs = wl.causal_pairs()
+    flops = FLOP_PER_PAIR_PER_HEAD_DIM * H * d * pairs
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nck)]
+          for _ in range(args.steps)]
+    for s_ev in ev:
+        for c_ev in s_ev:
+            for e in c_ev:
+                e.record(stream)
+
+    def step(evs=None, x=inp, on_chunk=None):
+        K.kpool_pool_keys(x["k"], x["cu_seqlens"], wl.kpool, out=kp, workspace=ws, stream=stream)
+        for c in range(nck):
+            lo, hi = bounds[c], bounds[c + 1]
+            buf = out[c % 2] if on_chunk is not None else out[0]
+            K.kpool_index_scores(x["q"], kp, x["w"], x["cu_seqlens"], wl.kpool, wl.scale, ld=ld, out=buf[:hi - lo],
+                                 row_range=(lo, hi), workspace=ws, stream=stream, pooled=True,
+                                 stage_events=None if evs is None else evs[c])
+            if on_chunk is not None:
+                on_chunk(c, buf[:hi - lo])
+
+    for _ in range(args.warmup):
+        step(ev[0])
+    torch.cuda.synchronize()
+    st = K.kpool_last_device_error(ws)
+    if st != K.KPOOL_OK:
+        raise K.KpoolError(st, "device (index scores)")
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    per = []
+    for s_i in range(args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step(ev[s_i])
+        b.record(stream)
+        per.append((a, b))
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop()
+    ms_step = max_over_ranks(statistics.median([a.elapsed_time(b) for a, b in per]), world)
+    value = world * pairs / (ms_step / 1e3)
+    k_ms = statistics.median([sum(c[2].elapsed_time(c[3]) for c in s_ev) for s_ev in ev])  # score kernels
+    setup_ms = statistics.median([sum(c[0].elapsed_time(c[2]) for c in s_ev) for s_ev in ev])  # plans
+    peaks = measured_peaks()
+    peak_burst = float(peaks["bf16_tflops"])
+    peak_sust = float(peaks.get("bf16_tflops_sustained", peak_burst))
+    hbm = float(peaks["hbm_gbs"])
+    achieved = flops / (k_ms / 1e3) / 1e12
+    out_bytes = T * ld * 4
+    alg_bytes = T * H * d * 2 + T * H * 4 + wl.num_pools() * d * 2 + out_bytes  # q, w, pooled keys in; scores out
+
+    # end to end: inputs from pinned host memory, every chunk's scores back to one pinned host
+    # buffer; chunk c+1 computes while chunk c downloads on a copy stream (two device buffers)
+    e2e = None
+    if not args.no_e2e:
+        keys = ("q", "k", "w", "cu_seqlens")
+        h_in = {k2: torch.empty(inp[k2].shape, dtype=inp[k2].dtype, pin_memory=True) for k2 in keys}
+        for k2 in keys:
+            h_in[k2].copy_(inp[k2])
+        d_in = {k2: torch.empty_like(inp[k2]) for k2 in keys}
+        h_out = torch.empty((chunk, ld), dtype=torch.float32, pin_memory=True)
+        copy = torch.cuda.Stream(device=dev)
+        bi = sum(v.numel() * v.element_size() for v in h_in.values())
+        freed = [None, None]  # event: the download of buffer i finished
+
+        def download(c, buf):
+            done = torch.cuda.Event()
+            done.record(stream)
+            copy.wait_event(done)
+            with torch.cuda.stream(copy):
+                h_out[:buf.shape[0]].copy_(buf, non_blocking=True)
+                f = torch.cuda.Event()
+                f.record(copy)
+            freed[c % 2] = f
+            nxt = freed[(c + 1) % 2]
+            if nxt is not None:
+                stream.wait_event(nxt)  # chunk c+1 writes the buffer chunk c-1 was downloaded from
+
+        e2e_t = []
+        for i in range(args.warmup + args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k2 in keys:
+                d_in[k2].copy_(h_in[k2], non_blocking=True)
+            freed[0] = freed[1] = None
+            step(None, d_in, download)
+            stream.wait_stream(copy)
+            b.record(stream)
+            e2e_t.append((a, b))
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(statistics.median([a.elapsed_time(b) for a, b in e2e_t[args.warmup:]]), world)
+        e2e = {"value": world * pairs / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": out_bytes, "ms_per_step": e2e_ms,
+               "d2h_GB/s": out_bytes / (e2e_ms / 1e3) / 1e9,
+               "pipelining": "each chunk's scores download on a copy stream while the next chunk computes"}
+        del h_in, d_in, h_out
+    line = {
+        "metric": SCORES_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": scores_config(wl, world, ld, chunk, nck),
+        "kernel_ms": {"plans": setup_ms, "index_scores": k_ms, "launches_per_step": nck},
+        "roofline": {"kernel": "select_tc_kernel (index-score mode)", "bound": "tensor", "achieved": achieved,
+                     "peak": peak_burst, "unit": "TFLOP/s", "frac": achieved / peak_burst, "traffic": None,
+                     "peak_kind": f"bf16 burst, {peaks['_source']}", "frac_of_sustained": achieved / peak_sust,
+                     "algorithmic_flop_per_launch": flops / nck, "algorithmic_bytes_per_launch": alg_bytes / nck,
+                     "output_GB/s": out_bytes / (k_ms / 1e3) / 1e9,
+                     "output_frac_of_hbm": out_bytes / (k_ms / 1e3) / 1e9 / hbm,
+                     "note": "per launch = the step's total over its chunk launches / launches"},
+        "clocks": clock_info,
+        "gpu_launches": (2 + 2 * nck) * args.steps,
+        "e2e": e2e,
+    }
+    traffic = NCU_TRAFFIC_SCORES
+    tc_src = os.path.join(ROOT, "sparse_attention_kpool_gb300", "csrc", "kpool_select_tc.cu")
+    if traffic["kernel_sha256"] == source_sha(tc_src) and traffic["workload"] == wl.name:
+        line["roofline"]["traffic"] = traffic["bytes_per_launch"]
+    if rank == 0 and not args.no_cpu:
+        from oracle import oracle
+        from tests import parity
+        oracle.build()
+        rows = pick_sample_rows(wl, args.cpu_sample_pairs / 4, seed=11)
+        cu = inp["cu_seqlens"].cpu().numpy()
+        kpo = oracle.pool(parity.bits(inp["k"]), wl.dtype, cu, wl.kpool)
+        t0 = time.perf_counter()
+        ref = parity.oracle_full_scores(inp, wl, rows, ld, kp=kpo)
+        dt = time.perf_counter() - t0
+        sp = int(np.isfinite(ref).sum())
+        line["cpu_baseline"] = {"value": sp / dt, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                                "sample": f"{len(rows)} uniform rows of {wl.name} ({sp:.3e} pairs, {dt:.1f} s, "
+                                          f"pooling excluded); fp64 scores"}
+        # the same rows as a parity spot check: each through its own one-row call
+        one = torch.empty((1, ld), dtype=torch.float32, device=dev)
+        got = np.empty((len(rows), ld), dtype=np.float32)
+        K.kpool_pool_keys(inp["k"], inp["cu_seqlens"], wl.kpool, out=kp, workspace=ws, stream=stream)
+        for i, r in enumerate(rows):
+            K.kpool_index_scores(inp["q"], kp, inp["w"], inp["cu_seqlens"], wl.kpool, wl.scale, ld=ld, out=one,
+                                 row_range=(int(r), int(r) + 1), workspace=ws, stream=stream, pooled=True)
+            got[i] = one.cpu().numpy()
+        ok = True
+        try:
+            err = parity.compare_full_scores(got, ref, exact=wl.values == "integer", what=wl.name)
+            line["parity_sample"] = {"rows": int(len(rows)), "ok": True, "max_rel_err": err}
+        except AssertionError as ex:
+            line["parity_sample"] = {"rows": int(len(rows)), "ok": False, "error": str(ex)[:200]}
+    if rank == 0 and emit:
+        print(json.dumps(line), flush=True)
+    del out, kp, inp, ws
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -473,6 +665,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the decode workload that the default (pages-scale) run also measures")
+    ap.add_argument("--index-scores", action="store_true",
+                    help="measure the full index-score output (kpool_index_scores) on --workload instead")
+    ap.add_argument("--no-index-scores", action="store_true",
+                    help="skip the index-score measurement that the default (pages-scale) run also makes")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -484,6 +680,12 @@ def main():
             dist.destroy_process_group()
         return
     wl = W.BY_NAME[args.workload]
+    if args.index_scores and args.impl == "ours":
+        index_scores_bench(args, wl, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if args.impl == "reference":
         reference_arm(args, wl, world, rank)
         if world > 1:
@@ -768,6 +970,15 @@ def main():
         line["decode_262k"] = {k: dec[k] for k in ("metric", "value", "unit", "ms_per_step", "us_per_decode_step",
                                                    "us_per_decode_step_graph", "kernel_ms", "roofline", "clocks",
                                                    "config", "e2e", "steps", "warmup")}
+    if wl.name == "pages_512k" and not args.no_index_scores:
+        # the full index-score output on long_128k (2 GiB chunks), measured in the same run;
+        # its oracle timing and parity sample run only standalone (--index-scores)
+        sc_args = argparse.Namespace(**vars(args))
+        sc_args.steps, sc_args.no_cpu = min(args.steps, 10), True
+        isc = index_scores_bench(sc_args, W.LONG_128K, world, rank, emit=False)
+        line["index_scores_long_128k"] = {k: isc[k] for k in ("metric", "value", "unit", "ms_per_step",
+                                                              "kernel_ms", "roofline", "clocks", "config", "e2e",
+                                                              "steps", "warmup")}
     if rank == 0 and not args.no_cpu:
         rows = pick_sample_rows(wl, args.cpu_sample_pairs, seed=7)
         res = oracle_sample(inp, wl, rows)

@@ -210,6 +210,43 @@ kpool_status kpool_select_pooled(const void* q, const void* pooled_keys, const f
                                  void* workspace, size_t workspace_bytes, void* stream,
                                  const kpool_options* options);
 /*
+ * Full index scores, the pages' return_index_scores output ("NVIDIA/Megatron-LM
+ * pull request #8299", section "Change": the op can return the index scores,
+ * which it computes in row chunks of at most 2 GiB). Writes step 2's score of
+ * every (row, pool) pair of a range of query rows instead of selecting:
+ *   out_scores  [R, ld] fp32 (device, 4-byte aligned), R = row_end - row_begin:
+ *               element (i, p), row i being global row row_begin + i (position t
+ *               of its sequence), is s[t,p] for the sequence's pool p when
+ *               p < floor((t+1)/kpool), and -INFINITY for every other p < ld.
+ *   ld          row stride in elements, >= 1. Every row of the range needs
+ *               ld >= floor((t+1)/kpool) (ld = floor(T/kpool) always suffices);
+ *               a row that is wider keeps its first ld scores and the call records
+ *               KPOOL_ERR_INVALID_ARG on the device (kpool_last_device_error).
+ *   options     as for kpool_select_ex: KPOOL_OPT_ROW_RANGE picks the rows (the
+ *               whole batch without it), so a caller bounds memory by calling once
+ *               per chunk of rows; score_kernel picks the family, and the scores
+ *               are bit-identical to the out_pool_scores a kpool_select_ex call with
+ *               the same score kernel returns for the pools it selects.
+ * q, k, w, cu_seqlens, the shape arguments, scale and the workspace are those of
+ * kpool_select (workspace: kpool_workspace_bytes(T, S, H, d, dtype, kpool, 0)).
+ * Supported shapes: the tensor-core kernel for bf16, H = 32, d = 128; the SIMT
+ * kernel for H <= 64, d <= 256. The 4th and 5th stage events are both recorded
+ * after the score kernel. An empty range or T = 0 is a no-op.
+ */
+kpool_status kpool_index_scores(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
+                                int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                                kpool_dtype dtype, int32_t kpool, float scale, float* out_scores, int64_t ld,
+                                void* workspace, size_t workspace_bytes, void* stream,
+                                const kpool_options* options);
+
+/* kpool_index_scores for pooled keys the caller already has (as kpool_select_pooled). */
+kpool_status kpool_index_scores_pooled(const void* q, const void* pooled_keys, const float* w,
+                                       const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                       int32_t heads, int32_t head_dim, kpool_dtype dtype, int32_t kpool, float scale,
+                                       float* out_scores, int64_t ld, void* workspace, size_t workspace_bytes,
+                                       void* stream, const kpool_options* options);
+
+/*
  * Step 4 alone: expands pool ids [T, budget] (as kpool_select writes them) into
  * token ids [T, index_topk + kpool], appending each row's tail and applying the
  * causal/varlen mask. Ids outside [0, floor((t+1)/kpool)) are treated as -1.

@@ -150,6 +150,99 @@ kpool_status select_check_args(const void* q, const void* kin, const float* w, c
 
 namespace {
 
+// The checks of kpool_index_scores(_pooled), in the order of select_check_args.
+kpool_status scores_check_args(const void* q, const void* kin, const float* w, const int32_t* cu_seqlens,
+                               int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                               kpool_dtype dtype, int32_t kpool, float scale, const float* out_scores, int64_t ld,
+                               const kpool_options* options, bool* use_tc, int64_t* row_begin, int64_t* row_end) {
+  kpool_options opt{};
+  if (options) opt = *options;
+  if (opt.reserved != 0 || (opt.flags & ~KPOOL_OPT_ROW_RANGE) != 0) return KPOOL_ERR_INVALID_ARG;
+  if (opt.score_kernel < KPOOL_SCORE_AUTO || opt.score_kernel > KPOOL_SCORE_SIMT || opt.max_ctas < 0)
+    return KPOOL_ERR_INVALID_ARG;
+  kpool_status st = check_shape(total_tokens, num_seqs, head_dim, dtype, kpool);
+  if (st != KPOOL_OK) return st;
+  if (heads < 1 || ld < 1 || !isfinite(scale)) return KPOOL_ERR_INVALID_ARG;
+  *row_begin = 0;
+  *row_end = total_tokens;
+  if (opt.flags & KPOOL_OPT_ROW_RANGE) {
+    if (opt.row_begin < 0 || opt.row_begin > opt.row_end || int64_t(opt.row_end) > total_tokens)
+      return KPOOL_ERR_INVALID_ARG;
+    *row_begin = opt.row_begin;
+    *row_end = opt.row_end;
+  } else if (opt.row_begin != 0 || opt.row_end != 0) {
+    return KPOOL_ERR_INVALID_ARG;
+  }
+  *use_tc = false;
+  if (total_tokens == 0 || *row_end == *row_begin) return KPOOL_OK;
+  if ((*row_end - *row_begin) > INT64_MAX / ld) return KPOOL_ERR_INVALID_ARG;  // R * ld elements
+  if (!q || !kin || !w || !cu_seqlens || !out_scores) return KPOOL_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kin, 16) || !aligned(w, 4) || !aligned(cu_seqlens, 4) || !aligned(out_scores, 4))
+    return KPOOL_ERR_INVALID_ARG;
+  const bool tc_ok = select_tc_supported(dtype, heads, head_dim, 1);
+  const bool simt_ok = heads <= 64 && head_dim <= 256;
+  switch (opt.score_kernel) {
+    case KPOOL_SCORE_TC:
+      if (!tc_ok) return KPOOL_ERR_UNSUPPORTED;
+      *use_tc = true;
+      break;
+    case KPOOL_SCORE_SIMT:
+      if (!simt_ok) return KPOOL_ERR_UNSUPPORTED;
+      break;
+    default:
+      if (!tc_ok && !simt_ok) return KPOOL_ERR_UNSUPPORTED;
+      *use_tc = tc_ok;
+  }
+  return KPOOL_OK;
+}
+
+// Index scores; pools k itself when `pooled_in` is null, else uses the caller's pooled keys.
+kpool_status scores_impl(const void* q, const void* k, const void* pooled_in, const float* w,
+                         const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t heads,
+                         int32_t head_dim, kpool_dtype dtype, int32_t kpool, float scale, float* out_scores,
+                         int64_t ld, void* workspace, size_t workspace_bytes, void* stream_ptr,
+                         const kpool_options* options) {
+  bool use_tc = false;
+  int64_t rb = 0, re = 0;
+  kpool_status st = scores_check_args(q, pooled_in ? pooled_in : k, w, cu_seqlens, num_seqs, total_tokens, heads,
+                                      head_dim, dtype, kpool, scale, out_scores, ld, options, &use_tc, &rb, &re);
+  if (st != KPOOL_OK) return st;
+  const int64_t T = total_tokens;
+  if (T == 0 || re == rb) return KPOOL_OK;
+  kpool_options opt{};
+  if (options) opt = *options;
+  const WorkspaceLayout L = workspace_layout(T, num_seqs, head_dim, elem_bytes(dtype), kpool);
+  st = check_workspace(workspace, workspace_bytes, L);
+  if (st != KPOOL_OK) return st;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int sms = 0;
+  if (!cuda_ok(sm_count(&sms))) return KPOOL_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  const void* pooled = pooled_in ? pooled_in : static_cast<const void*>(ws + L.pooled);
+  void* const* ev = opt.stage_events;
+  auto mark = [&](int i) {
+    return ev == nullptr || cuda_ok(record_stage_event(ev[i], stream));
+  };
+  if (!mark(0)) return KPOOL_ERR_CUDA;
+  if (!cuda_ok(launch_plan(cu_seqlens, num_seqs, T, kpool, rb, re, ws, L, stream)) || !mark(1)) return KPOOL_ERR_CUDA;
+  if (!pooled_in &&
+      !cuda_ok(launch_pool(k, dtype, cu_seqlens, num_seqs, T, head_dim, kpool, ws + L.pooled, ws, L, sms, stream)))
+    return KPOOL_ERR_CUDA;
+  if (!mark(2)) return KPOOL_ERR_CUDA;
+  cudaError_t e;
+  if (use_tc) {
+    int grid = sms;
+    if (opt.max_ctas > 0 && opt.max_ctas < grid) grid = opt.max_ctas;
+    e = launch_scores_tc(q, pooled, w, cu_seqlens, T, kpool, scale, rb, re, out_scores, ld, ws, L, grid, stream);
+  } else {
+    e = launch_scores_simt(q, pooled, w, dtype, cu_seqlens, num_seqs, T, heads, head_dim, kpool, scale, rb, re,
+                           out_scores, ld, ws, L, opt.max_ctas > 0 ? opt.max_ctas : sms, stream);
+  }
+  if (!cuda_ok(e) || !mark(3) || !mark(4)) return KPOOL_ERR_CUDA;
+  return KPOOL_OK;
+}
+
 // The whole selection; pools k itself when `pooled_in` is null, else scores the
 // caller's pooled keys (k unused).
 kpool_status select_impl(const void* q, const void* k, const void* pooled_in, const float* w,
@@ -236,6 +329,24 @@ kpool_status kpool_select_pooled(const void* q, const void* pooled_keys, const f
   return select_impl(q, nullptr, pooled_keys, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool,
                      index_topk, scale, out_pool_ids, out_token_ids, out_pool_scores, workspace, workspace_bytes,
                      stream_ptr, options);
+}
+
+kpool_status kpool_index_scores(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,
+                                int32_t num_seqs, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                                kpool_dtype dtype, int32_t kpool, float scale, float* out_scores, int64_t ld,
+                                void* workspace, size_t workspace_bytes, void* stream,
+                                const kpool_options* options) {
+  return scores_impl(q, k, nullptr, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool, scale,
+                     out_scores, ld, workspace, workspace_bytes, stream, options);
+}
+
+kpool_status kpool_index_scores_pooled(const void* q, const void* pooled_keys, const float* w,
+                                       const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                       int32_t heads, int32_t head_dim, kpool_dtype dtype, int32_t kpool, float scale,
+                                       float* out_scores, int64_t ld, void* workspace, size_t workspace_bytes,
+                                       void* stream, const kpool_options* options) {
+  return scores_impl(q, nullptr, pooled_keys, w, cu_seqlens, num_seqs, total_tokens, heads, head_dim, dtype, kpool,
+                     scale, out_scores, ld, workspace, workspace_bytes, stream, options);
 }
 
 kpool_status kpool_select(const void* q, const void* k, const float* w, const int32_t* cu_seqlens,

@@ -139,6 +139,17 @@ cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, cons
                              int64_t row_end, int32_t* out_ids, float* out_scores, char* ws,
                              const WorkspaceLayout& L, int grid, cudaStream_t stream);
 
+// Index scores (kpool_index_scores): the score of every (row, pool) pair of the global
+// rows [row_begin, row_end) into out_scores [R, ld] (-inf where the pool is not
+// eligible), with the same arithmetic as the selection kernel of the same family.
+cudaError_t launch_scores_tc(const void* q, const void* kp, const float* w, const int32_t* cu, int64_t T,
+                             int32_t kpool, float scale, int64_t row_begin, int64_t row_end, float* out_scores,
+                             int64_t ld, char* ws, const WorkspaceLayout& L, int grid, cudaStream_t stream);
+cudaError_t launch_scores_simt(const void* q, const void* kp, const float* w, kpool_dtype dtype, const int32_t* cu,
+                               int32_t S, int64_t T, int32_t H, int32_t d, int32_t kpool, float scale,
+                               int64_t row_begin, int64_t row_end, float* out_scores, int64_t ld, char* ws,
+                               const WorkspaceLayout& L, int num_sms, cudaStream_t stream);
+
 // K3: pool ids -> token ids for the global rows [row_begin, row_end) (pool_ids and
 // out_tokens hold those rows only). `hdr` may be null; when given, the kernel does
 // nothing if the planning kernel recorded an error.

@@ -26,6 +26,22 @@ namespace {
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// s[t,p] of one (row, pool) pair: an fp32 FMA chain over the channels per head, then
+// an FMA of |scale| * w[h] and the surviving side of zero per head. The selection
+// and the index-score kernels both call this, so their scores agree bit for bit.
+template <typename T, bool kNegScale>
+__device__ __forceinline__ float simt_score(const T* __restrict__ qr, const T* __restrict__ kr,
+                                            const float* __restrict__ wr, int H, int d, float abs_scale) {
+  float s = 0.0f;
+  for (int h = 0; h < H; ++h) {
+    float dot = 0.0f;
+    for (int c = 0; c < d; ++c) dot = fmaf(to_f32(qr[h * d + c]), to_f32(kr[c]), dot);
+    const float v = kNegScale ? -dot : dot;
+    s = fmaf(__ldg(wr + h) * abs_scale, fmaxf(v, 0.0f), s);
+  }
+  return s;
+}
+
 template <typename T, bool kNegScale>
 __global__ void __launch_bounds__(128) select_simt_kernel(
     const T* __restrict__ q, const T* __restrict__ kp, const float* __restrict__ w,
@@ -55,17 +71,7 @@ __global__ void __launch_bounds__(128) select_simt_kernel(
     for (int64_t p0 = 0; p0 < eligible; p0 += 32) {
       const int64_t p = p0 + lane;
       uint64_t key = 0;
-      if (p < eligible) {
-        const T* kr = kseq + p * d;
-        float s = 0.0f;
-        for (int h = 0; h < H; ++h) {
-          float dot = 0.0f;
-          for (int c = 0; c < d; ++c) dot = fmaf(to_f32(qr[h * d + c]), to_f32(kr[c]), dot);
-          const float v = kNegScale ? -dot : dot;
-          s = fmaf(__ldg(wr + h) * abs_scale, fmaxf(v, 0.0f), s);
-        }
-        key = make_key(s, uint32_t(p));
-      }
+      if (p < eligible) key = make_key(simt_score<T, kNegScale>(qr, kseq + p * d, wr, H, d, abs_scale), uint32_t(p));
       const bool pass = key > tau;
       const unsigned m = __ballot_sync(0xffffffffu, pass);
       if (pass) buf[count + __popc(m & lt_mask)] = key;
@@ -91,6 +97,35 @@ __global__ void __launch_bounds__(128) select_simt_kernel(
       if (out_scores) out_scores[orow * budget + j] = key ? key_score(key) : -INFINITY;
     }
     __syncwarp();
+  }
+}
+
+// Index scores on CUDA cores: one warp per row of [row_begin, row_end), lanes over
+// the pools 0 .. ld-1 of the row's sequence; eligible pools get simt_score, every
+// other column -inf.
+template <typename T, bool kNegScale>
+__global__ void __launch_bounds__(128) scores_simt_kernel(
+    const T* __restrict__ q, const T* __restrict__ kp, const float* __restrict__ w,
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ pool_off, WorkspaceHeader* __restrict__ hdr,
+    int S, int64_t row_begin, int64_t row_end, int H, int d, int kpool, float abs_scale,
+    float* __restrict__ out, int64_t ld) {
+  // planning failed (malformed cu_seqlens); n_items, unlike the error word, is not
+  // written again during this kernel, so every block takes the same decision
+  if (hdr->n_items == 0) return;
+  const int lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  for (int64_t row = row_begin + int64_t(blockIdx.x) * warps + (threadIdx.x >> 5); row < row_end;
+       row += int64_t(gridDim.x) * warps) {
+    const int b = seq_of_row(cu, S, row);
+    const int64_t t = row - __ldg(cu + b);
+    const int64_t eligible = (t + 1) / kpool;
+    if (eligible > ld && lane == 0) record_error(hdr, KPOOL_ERR_INVALID_ARG);  // row wider than ld
+    const T* qr = q + row * int64_t(H) * d;
+    const float* wr = w + row * int64_t(H);
+    const T* kseq = kp + int64_t(__ldg(pool_off + b)) * d;
+    float* o = out + (row - row_begin) * ld;
+    for (int64_t p = lane; p < ld; p += 32)
+      __stcs(o + p, p < eligible ? simt_score<T, kNegScale>(qr, kseq + p * d, wr, H, d, abs_scale) : -INFINITY);
   }
 }
 
@@ -145,6 +180,43 @@ cudaError_t launch_select_simt(const void* q, const void* kp, const float* w, kp
                                          ws, L, num_sms, stream)
              : launch_typed<float, false>(q, kp, w, cu, S, rb, re, H, d, kpool, budget, abs_scale, out_ids,
                                           out_scores, ws, L, num_sms, stream);
+}
+
+cudaError_t launch_scores_simt(const void* q, const void* kp, const float* w, kpool_dtype dtype, const int32_t* cu,
+                               int32_t S, int64_t T, int32_t H, int32_t d, int32_t kpool, float scale,
+                               int64_t row_begin, int64_t row_end, float* out_scores, int64_t ld, char* ws,
+                               const WorkspaceLayout& L, int num_sms, cudaStream_t stream) {
+  if (T == 0 || row_end <= row_begin) return cudaSuccess;
+  const bool neg = scale < 0.0f;
+  const float abs_scale = neg ? -scale : scale;
+  constexpr int kWarps = 4;
+  int64_t blocks = (row_end - row_begin + kWarps - 1) / kWarps;
+  if (blocks > int64_t(num_sms) * 16) blocks = int64_t(num_sms) * 16;
+  const int32_t* po = reinterpret_cast<const int32_t*>(ws + L.pool_off);
+  WorkspaceHeader* hdr = reinterpret_cast<WorkspaceHeader*>(ws + L.header);
+  const unsigned g = unsigned(blocks);
+  if (dtype == KPOOL_BF16) {
+    const auto* qq = static_cast<const __nv_bfloat16*>(q);
+    const auto* kk = static_cast<const __nv_bfloat16*>(kp);
+    if (neg)
+      scores_simt_kernel<__nv_bfloat16, true><<<g, 32 * kWarps, 0, stream>>>(qq, kk, w, cu, po, hdr, S, row_begin,
+                                                                           row_end, H, d, kpool, abs_scale,
+                                                                           out_scores, ld);
+    else
+      scores_simt_kernel<__nv_bfloat16, false><<<g, 32 * kWarps, 0, stream>>>(qq, kk, w, cu, po, hdr, S, row_begin,
+                                                                            row_end, H, d, kpool, abs_scale,
+                                                                            out_scores, ld);
+  } else {
+    const auto* qq = static_cast<const float*>(q);
+    const auto* kk = static_cast<const float*>(kp);
+    if (neg)
+      scores_simt_kernel<float, true><<<g, 32 * kWarps, 0, stream>>>(qq, kk, w, cu, po, hdr, S, row_begin, row_end, H,
+                                                                   d, kpool, abs_scale, out_scores, ld);
+    else
+      scores_simt_kernel<float, false><<<g, 32 * kWarps, 0, stream>>>(qq, kk, w, cu, po, hdr, S, row_begin, row_end,
+                                                                    H, d, kpool, abs_scale, out_scores, ld);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace kpool

@@ -50,6 +50,15 @@
 // is cut to exactly `budget` keys the same way, then one warp per row sorts them
 // in registers (bitonic) and writes the ranked ids.
 //
+// Index-score mode (kScores): the same producer, MMA issuer and scoring loop,
+// but every epilogue thread stores its fp32 score to a [rows, ld] matrix (-inf
+// where the pool is not eligible) instead of filtering it, and after an item's
+// tiles the group writes -inf to the rest of its rows. This is the pages' full
+// score output ("NVIDIA/Megatron-LM pull request #8299", section "Change":
+// return_index_scores), bounded by the caller's row range as the pages bound
+// their score chunks. The scores are bit-identical to the ones the selection
+// ranks.
+//
 // The producer and MMA roles, the cooperative compaction and the final ranking
 // are noinline functions: kept out of the kernel body, their code does not shape
 // the register allocation of the epilogue's scoring loop (measured: 4-5 % faster at
@@ -412,14 +421,16 @@ __device__ __noinline__ void mma_role(const int32_t* cu, const int32_t* pool_off
   ptx::mbar_wait_bounded(bar.mma_done, 0, kMaxPolls, kMaxWaitNs);
 }
 
-template <bool kNegScale>
+// kScores = false: selection (out_ids [R, budget], out_scores [R, budget] or null).
+// kScores = true: index scores (out_scores [R, ld]; out_ids and budget unused).
+template <bool kNegScale, bool kScores>
 __global__ void __launch_bounds__(kThreads, 1)
     select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
                      const float* __restrict__ w, const int32_t* __restrict__ cu,
                      const int32_t* __restrict__ pool_off, const int2* __restrict__ items,
                      WorkspaceHeader* __restrict__ hdr, int kpool, int budget, float abs_scale,
                      int64_t row_begin, int64_t row_end, int32_t* __restrict__ out_ids,
-                     float* __restrict__ out_scores) {
+                     float* __restrict__ out_scores, int64_t ld) {
   // Pointers derived directly from the __shared__ array keep the shared address
   // space, so the compiler emits shared loads, stores and atomics (LDS/STS/ATOMS)
   // rather than generic ones.
@@ -533,8 +544,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gt < 4) {
         const int q = rbase + gt;
         const int row = it.t0 + q;
-        s_tau[q] = 0;
         s_elig[q] = row < it.len ? (row + 1) / kpool : 0;
+        if constexpr (kScores) {
+          // the output row, or -1 for rows past the sequence or outside the range
+          const int64_t grow = it.seq_start + row;
+          const bool written = row < it.len && grow >= row_begin && grow < row_end;
+          s_tau[q] = written ? uint64_t(grow - row_begin) : ~0ull;
+          if (written && s_elig[q] > ld) record_error(hdr, KPOOL_ERR_INVALID_ARG);  // row wider than ld
+        } else {
+          s_tau[q] = 0;
+        }
       }
       int cnt[4] = {0, 0, 0, 0};  // this warp's region counts of the group's four rows
       named_bar(bar_id, 128);
@@ -605,9 +624,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::unpack_f32x2(acc0, s0, s1);
             ptx::unpack_f32x2(acc1, s2, s3);
             const float s = (s0 + s1) + (s2 + s3);
-            key[j] = make_key(s, uint32_t(p));
-            pass[j] = p < s_elig[q] && key[j] > s_tau[q];
-            m[j] = __ballot_sync(0xffffffffu, pass[j]);
+            if constexpr (kScores) {
+              const int64_t orow = int64_t(s_tau[q]);
+              if (orow >= 0 && p < ld) __stcs(out_scores + orow * ld + p, p < s_elig[q] ? s : -INFINITY);
+            } else {
+              key[j] = make_key(s, uint32_t(p));
+              pass[j] = p < s_elig[q] && key[j] > s_tau[q];
+              m[j] = __ballot_sync(0xffffffffu, pass[j]);
+            }
             if (j < 3) {
               ptx::tc_wait_ld();
               ptx::tc_reg_fence(v[(j + 1) & 1]);
@@ -617,14 +641,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // A region holds at most kRegMark keys when a tile starts (a compaction runs as
           // soon as one passes the mark) and a tile adds at most 32, so every slot below
           // is < kReg without a per-key check.
+          if constexpr (!kScores) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (pass[j]) my_region[j * kCap + cnt[j] + __popc(m[j] & lt_mask)] = key[j];
-            cnt[j] += __popc(m[j]);
+            for (int j = 0; j < 4; ++j) {
+              if (pass[j]) my_region[j * kCap + cnt[j] + __popc(m[j] & lt_mask)] = key[j];
+              cnt[j] += __popc(m[j]);
+            }
+            const int cmax = max(max(cnt[0], cnt[1]), max(cnt[2], cnt[3]));
+            over = cmax > kRegMark;
+            overflow = overflow || cmax > kReg;  // cannot happen; reported at the end of the item
           }
-          const int cmax = max(max(cnt[0], cnt[1]), max(cnt[2], cnt[3]));
-          over = cmax > kRegMark;
-          overflow = overflow || cmax > kReg;  // cannot happen; reported at the end of the item
         }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
@@ -651,6 +677,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (aborted) break;
+      if constexpr (kScores) {
+        // the pools no tile covered: -inf up to ld for each of the group's rows
+        const int64_t p_from = int64_t(it.n_tiles) * kTilePools;
+        for (int j = 0; j < 4; ++j) {
+          const int64_t orow = int64_t(s_tau[rbase + j]);
+          if (orow >= 0)
+            for (int64_t pp = p_from + gt; pp < ld; pp += 128) __stcs(out_scores + orow * ld + pp, -INFINITY);
+        }
+        named_bar(bar_id, 128);  // the item's row state is read above; the next item rewrites it
+        continue;
+      }
       if (overflow && lane == 0) record_error(hdr, KPOOL_ERR_INTERNAL);
       // final ranking: cut each of the group's rows to its top `budget` keys, dealt
       // evenly over the four regions (the group's four warps together), then warp wq
@@ -727,7 +764,7 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_ro
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool g_attr_set[64][2] = {};
+bool g_attr_set[64][4] = {};
 
 }  // namespace
 
@@ -735,11 +772,12 @@ bool select_tc_supported(kpool_dtype dtype, int32_t H, int32_t d, int32_t budget
   return dtype == KPOOL_BF16 && H == kHeads && d == kDim && budget >= 1 && budget <= kMaxBudget;
 }
 
-cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, const int32_t* cu, int32_t S, int64_t T,
-                             int32_t kpool, int32_t budget, float scale, int64_t row_begin, int64_t row_end,
-                             int32_t* out_ids, float* out_scores, char* ws, const WorkspaceLayout& L, int grid,
-                             cudaStream_t stream) {
-  (void)S;
+namespace {
+
+cudaError_t launch_tc(bool scores, const void* q, const void* kp, const float* w, const int32_t* cu, int64_t T,
+                      int32_t kpool, int32_t budget, float scale, int64_t row_begin, int64_t row_end, int32_t* out_ids,
+                      float* out_scores, int64_t ld, char* ws, const WorkspaceLayout& L, int grid,
+                      cudaStream_t stream) {
   if (T == 0 || row_end <= row_begin) return cudaSuccess;
   if (T * kHeads > int64_t(INT32_MAX)) return cudaErrorInvalidValue;
   CUtensorMap map_q, map_kp;
@@ -748,20 +786,40 @@ cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, cons
   if (!make_map(&map_kp, kp, kp_rows, kTilePools)) return cudaErrorInvalidValue;
   const bool neg = scale < 0.0f;
   const float abs_scale = neg ? -scale : scale;
-  auto kern = neg ? select_tc_kernel<true> : select_tc_kernel<false>;
+  auto kern = scores ? (neg ? select_tc_kernel<true, true> : select_tc_kernel<false, true>)
+                     : (neg ? select_tc_kernel<true, false> : select_tc_kernel<false, false>);
+  const int variant = (neg ? 1 : 0) + (scores ? 2 : 0);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !g_attr_set[dev][neg ? 1 : 0]) {
+  if (dev < 0 || dev >= 64 || !g_attr_set[dev][variant]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) g_attr_set[dev][neg ? 1 : 0] = true;
+    if (dev >= 0 && dev < 64) g_attr_set[dev][variant] = true;
   }
   kern<<<grid, kThreads, kSmemBytes, stream>>>(
       map_q, map_kp, w, cu, reinterpret_cast<const int32_t*>(ws + L.pool_off),
       reinterpret_cast<const int2*>(ws + L.items), reinterpret_cast<WorkspaceHeader*>(ws + L.header), kpool, budget,
-      abs_scale, row_begin, row_end, out_ids, out_scores);
+      abs_scale, row_begin, row_end, out_ids, out_scores, ld);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_select_tc(const void* q, const void* kp, const float* w, const int32_t* cu, int32_t S, int64_t T,
+                             int32_t kpool, int32_t budget, float scale, int64_t row_begin, int64_t row_end,
+                             int32_t* out_ids, float* out_scores, char* ws, const WorkspaceLayout& L, int grid,
+                             cudaStream_t stream) {
+  (void)S;
+  return launch_tc(false, q, kp, w, cu, T, kpool, budget, scale, row_begin, row_end, out_ids, out_scores, 0, ws, L,
+                   grid, stream);
+}
+
+cudaError_t launch_scores_tc(const void* q, const void* kp, const float* w, const int32_t* cu, int64_t T,
+                             int32_t kpool, float scale, int64_t row_begin, int64_t row_end, float* out_scores,
+                             int64_t ld, char* ws, const WorkspaceLayout& L, int grid, cudaStream_t stream) {
+  return launch_tc(true, q, kp, w, cu, T, kpool, 0, scale, row_begin, row_end, nullptr, out_scores, ld, ws, L, grid,
+                   stream);
 }
 
 }  // namespace kpool

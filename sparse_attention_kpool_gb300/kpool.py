@@ -40,7 +40,7 @@ EXPORTED = (
     "kpool_last_device_error", "kpool_wait_timeout_selftest", "kpool_status_string", "kpool_last_cuda_error",
     "kpool_select_static_scratch", "kpool_rows_workspace_bytes", "kpool_select_rows", "kpool_select_rows_ex",
     "kpool_pool_keys_gated", "kpool_select_pooled", "kpool_static_scratch_last_device_error",
-    "kpool_balanced_row_split",
+    "kpool_balanced_row_split", "kpool_index_scores", "kpool_index_scores_pooled",
 )
 KPOOL_STATIC_SCRATCH_BYTES = 48 << 20
 
@@ -116,6 +116,11 @@ def load() -> ctypes.CDLL:
         lib.kpool_select_pooled.restype = i32
         lib.kpool_balanced_row_split.argtypes = [P, i32, i32, i64, i32, P]
         lib.kpool_balanced_row_split.restype = i32
+        isc = [P, P, P, P, i32, i64, i32, i32, i32, i32, f32, P, i64, P, sz, P, ctypes.POINTER(kpool_options)]
+        lib.kpool_index_scores.argtypes = isc
+        lib.kpool_index_scores.restype = i32
+        lib.kpool_index_scores_pooled.argtypes = isc
+        lib.kpool_index_scores_pooled.restype = i32
         _lib = lib
         return lib
 
@@ -194,17 +199,7 @@ def kpool_select_ex(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, cu_seqlen
     if workspace is None:
         workspace = new_workspace(T, S, H, d, dt, kpool, index_topk, dev)
     _check_cuda(q, k, w, cu_seqlens, out_pool_ids, out_token_ids, out_pool_scores, workspace)
-    opts = kpool_options(score_kernel, max_ctas)
-    if row_range is not None:
-        opts.row_begin, opts.row_end = int(row_range[0]), int(row_range[1])
-        opts.flags = KPOOL_OPT_ROW_RANGE
-    if stage_events is not None:
-        if len(stage_events) != 5:
-            raise ValueError("stage_events needs 5 events")
-        arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(int(e.cuda_event)) for e in stage_events])
-        if not all(arr):
-            raise ValueError("record each event once before passing it (torch creates events lazily)")
-        opts.stage_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    opts, _arr = _options(score_kernel, max_ctas, row_range, stage_events)
     st = load().kpool_select_ex(_ptr(q), _ptr(k), _ptr(w), _ptr(cu_seqlens), S, T, H, d, dt, kpool, index_topk,
                                 float(scale), _ptr(out_pool_ids), _ptr(out_token_ids), _ptr(out_pool_scores),
                                 _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts))
@@ -406,6 +401,56 @@ def kpool_select_pooled(q: torch.Tensor, pooled_keys: torch.Tensor, w: torch.Ten
     if st != KPOOL_OK:
         raise KpoolError(st, "kpool_select_pooled")
     return out_pool_ids, out_token_ids, out_pool_scores
+
+
+def _options(score_kernel, max_ctas, row_range, stage_events):
+    """kpool_options for a call, plus the event array it points to (keep both alive)."""
+    opts = kpool_options(score_kernel, max_ctas)
+    if row_range is not None:
+        opts.row_begin, opts.row_end = int(row_range[0]), int(row_range[1])
+        opts.flags = KPOOL_OPT_ROW_RANGE
+    arr = None
+    if stage_events is not None:
+        if len(stage_events) != 5:
+            raise ValueError("stage_events needs 5 events")
+        arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(int(e.cuda_event)) for e in stage_events])
+        if not all(arr):
+            raise ValueError("record each event once before passing it (torch creates events lazily)")
+        opts.stage_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    return opts, arr
+
+
+def kpool_index_scores(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, cu_seqlens: torch.Tensor, kpool: int,
+                       scale: float, ld: int | None = None, out=None, row_range=None, workspace=None, stream=None,
+                       score_kernel: int = KPOOL_SCORE_AUTO, max_ctas: int = 0, stage_events=None,
+                       pooled: bool = False):
+    """Full index scores [R, ld] fp32 of the rows [row_begin, row_end) (all T rows without
+    row_range): element (i, p) is the score of pool p of the row's sequence when the row may
+    see it, else -inf. ld defaults to T // kpool. With pooled=True, `k` holds pooled keys
+    (kpool_index_scores_pooled)."""
+    T, H, d = q.shape
+    S = cu_seqlens.numel() - 1
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or w.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("k must match q's dtype; w must be float32; cu_seqlens int32")
+    if ld is None:
+        ld = max(1, T // kpool) if kpool > 0 else 1
+    R = T if row_range is None else max(0, int(row_range[1]) - int(row_range[0]))
+    dev = q.device
+    if out is None:
+        out = torch.empty((R, ld), dtype=torch.float32, device=dev)
+    elif out.dtype != torch.float32 or out.numel() < R * ld or not out.is_contiguous():
+        raise TypeError("out must be a contiguous float32 tensor of at least R * ld elements")
+    if workspace is None:
+        workspace = new_workspace(T, S, H, d, dt, kpool, 0, dev)
+    _check_cuda(q, k, w, cu_seqlens, out, workspace)
+    opts, _arr = _options(score_kernel, max_ctas, row_range, stage_events)
+    fn = load().kpool_index_scores_pooled if pooled else load().kpool_index_scores
+    st = fn(_ptr(q), _ptr(k), _ptr(w), _ptr(cu_seqlens), S, T, H, d, dt, kpool, float(scale), _ptr(out), int(ld),
+            _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts))
+    if st != KPOOL_OK:
+        raise KpoolError(st, "kpool_index_scores")
+    return out
 
 
 def kpool_balanced_row_split(cu_seqlens, kpool: int, parts: int, row_weight: int = 0) -> list:

@@ -121,6 +121,47 @@ def compare_float(inp: dict, wl, ref: dict, gpu_ids: np.ndarray, gpu_scores: np.
             "scores_compared": scores_compared}
 
 
+def oracle_full_scores(inp: dict, wl, rows: np.ndarray, ld: int, kp: np.ndarray | None = None) -> np.ndarray:
+    """The oracle's fp64 score of every pool of the listed global rows as an [n, ld] matrix,
+    -inf where the pool is not eligible: the oracle's selection with a budget as large as
+    the batch's pool count keeps (and scores) every eligible pool of a row."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cu = inp["cu_seqlens"].cpu().numpy()
+    if kp is None:
+        kp = oracle.pool(bits(inp["k"]), wl.dtype, cu, wl.kpool)
+    every = max(1, wl.total_tokens // wl.kpool)
+    ridx = torch.as_tensor(rows, device=inp["q"].device)
+    sel = oracle.select(bits(inp["q"][ridx]), inp["w"][ridx].cpu().numpy(), kp, cu, rows, wl.dtype, wl.kpool,
+                        wl.kpool * every, wl.scale)
+    full = np.full((len(rows), ld), -np.inf)
+    for i in range(len(rows)):
+        ids = sel["pool_ids"][i]
+        m = ids >= 0
+        assert int(m.sum()) == int(sel["eligible"][i])
+        keep = ids[m] < ld
+        full[i, ids[m][keep]] = sel["scores"][i, m][keep]
+    return full
+
+
+def compare_full_scores(gpu: np.ndarray, ref: np.ndarray, exact: bool, what: str = "") -> float:
+    """Index scores against the oracle's: -inf in exactly the same places, and every finite
+    score equal (exact) or within TOL_REL * max(|s_ref|, 1e-3 * rowmax |s_ref|). Returns the
+    largest relative error seen."""
+    assert gpu.shape == ref.shape
+    fin = np.isfinite(ref)
+    np.testing.assert_array_equal(np.isfinite(gpu), fin, err_msg=f"{what}: eligible pattern")
+    assert (gpu[~fin] == -np.inf).all(), f"{what}: non-eligible pools must be -inf"
+    if exact:
+        np.testing.assert_array_equal(gpu[fin].astype(np.float64), ref[fin], err_msg=f"{what}: scores")
+        return 0.0
+    rowmax = np.max(np.where(fin, np.abs(ref), 0.0), axis=1, keepdims=True)
+    base = np.maximum(np.maximum(np.abs(ref), 1e-3 * rowmax), 1e-30)[fin]
+    err = np.abs(gpu.astype(np.float64)[fin] - ref[fin]) / base
+    worst = float(err.max()) if err.size else 0.0
+    assert worst <= TOL_REL, f"{what}: relative score error {worst:.3e} > {TOL_REL}"
+    return worst
+
+
 def cutoff_tie_rows(ref_wide: dict, budget: int) -> np.ndarray:
     """Rows (indices into ref_wide) where an exact tie straddles the budget cutoff: the
     budget-th and (budget+1)-th ranked scores are equal, so the tiebreak alone decides

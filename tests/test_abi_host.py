@@ -241,6 +241,54 @@ def test_row_range_validation(lib):
                                     ctypes.byref(o)) == K.KPOOL_ERR_INVALID_ARG
 
 
+def _scores(lib, T=64, S=1, H=4, d=32, dtype=K.KPOOL_F32, kpool=4, scale=0.5, q=FAKE, k=FAKE, w=FAKE, cu=FAKE,
+            out=FAKE, ld=16, ws=FAKE, ws_bytes=1 << 30, opts=None, pooled=False):
+    P = ctypes.c_void_p
+    fn = lib.kpool_index_scores_pooled if pooled else lib.kpool_index_scores
+    return fn(P(q), P(k), P(w), P(cu), S, T, H, d, dtype, kpool, scale, P(out), ld, P(ws), ws_bytes, None,
+              ctypes.byref(opts) if opts else None)
+
+
+@pytest.mark.parametrize("pooled", [False, True])
+def test_index_scores_validation(lib, pooled):
+    def sc(**kw):
+        return _scores(lib, pooled=pooled, **kw)
+    assert sc(kpool=0) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(H=0) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(d=30) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(ld=0) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(ld=-3) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(ld=1 << 62) == K.KPOOL_ERR_INVALID_ARG             # R * ld elements overflow
+    assert sc(scale=float("nan")) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(out=0) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(out=FAKE + 2) == K.KPOOL_ERR_INVALID_ARG             # fp32 alignment
+    assert sc(k=0) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(k=FAKE + 8) == K.KPOOL_ERR_INVALID_ARG               # 16-byte rows
+    assert sc(ws=0) == K.KPOOL_ERR_WORKSPACE
+    assert sc(ws_bytes=1024) == K.KPOOL_ERR_WORKSPACE
+    assert sc(T=0, S=0, q=0, k=0, w=0, cu=0, out=0, ws=0) == K.KPOOL_OK
+    # row ranges as for kpool_select_ex; an empty one is a no-op
+    assert sc(opts=_range_opts(10, 9)) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(opts=_range_opts(0, 65)) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(opts=_range_opts(0, 10, flags=0)) == K.KPOOL_ERR_INVALID_ARG
+    assert sc(out=0, ws=0, opts=_range_opts(9, 9)) == K.KPOOL_OK
+    assert sc(ws=0, opts=_range_opts(0, 32)) == K.KPOOL_ERR_WORKSPACE
+    # the tensor-core kernel needs bf16, H = 32, d = 128; the SIMT one H <= 64, d <= 256
+    assert sc(opts=K.kpool_options(K.KPOOL_SCORE_TC, 0)) == K.KPOOL_ERR_UNSUPPORTED
+    assert sc(H=65, d=128, dtype=K.KPOOL_BF16) == K.KPOOL_ERR_UNSUPPORTED
+    assert sc(H=32, d=128, dtype=K.KPOOL_BF16, ws=0, opts=K.kpool_options(K.KPOOL_SCORE_TC, 0)) == \
+        K.KPOOL_ERR_WORKSPACE
+    bad = K.kpool_options(K.KPOOL_SCORE_AUTO, 0)
+    bad.reserved = 1
+    assert sc(opts=bad) == K.KPOOL_ERR_INVALID_ARG
+
+
+def test_index_scores_workspace_is_the_selections(lib):
+    # the index-score calls take the selection's workspace; index_topk 0 sizes it
+    assert K.kpool_workspace_bytes(8192, 2, 32, 128, K.KPOOL_BF16, 4, 0) == \
+        K.kpool_workspace_bytes(8192, 2, 32, 128, K.KPOOL_BF16, 4, 2048)
+
+
 def _pairs_per_row(cu, kpool):
     rows = []
     for b in range(len(cu) - 1):
