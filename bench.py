@@ -495,7 +495,9 @@ def index_scores_bench(args, wl: W.Workload, world: int, rank: int, emit: bool =
     nck = len(bounds) - 1
     dt_code = K.KPOOL_BF16 if wl.dtype == "bf16" else K.KPOOL_F32
     ws = K.new_workspace(T, wl.num_seqs, H, d, dt_code, wl.kpool, 0, dev)
-    out = [torch.empty((chunk, ld), dtype=torch.float32, device=dev) for _ in range(2)]
+    out = [torch.empty((chunk, ld), dtype=torch.float32, device=dev)]
+    if not args.no_e2e:
+        out.append(torch.empty((chunk, ld), dtype=torch.float32, device=dev))  # double buffer for the downloads
     kp = torch.empty((max(1, T // wl.kpool), d), dtype=inp["k"].dtype, device=dev)
     pairs = wl.causal_pairs()
     flops = FLOP_PER_PAIR_PER_HEAD_DIM * H * d * pairs
