@@ -560,6 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool aborted = false;
       bool overflow = false;  // a region passed its capacity (a library bug; see the insertion)
       for (int i = 0; i < it.n_tiles; ++i) {
+        if constexpr (kScores) {
+          if (*abort_flag != 0) {  // another role gave up: leave the tiles, the item-end vote follows
+            aborted = true;
+            break;
+          }
+        }
         bool over = false;  // this warp's reservation pushed a row past the compaction mark
         // every lane tests the barrier (one warp-wide instruction, no divergent branch);
         // the vote keeps a wait that ran out uniform across the warp
@@ -654,6 +660,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
+        if constexpr (kScores) {
+          // no shared state changes between tiles: the warps run free, paced by the
+          // accumulator barriers, and vote once at the end of the item
+          if (!ready) {
+            aborted = true;
+            break;
+          }
+          continue;
+        }
         // one group barrier per tile in the common case; its OR says whether any of the
         // group's rows needs compacting or a wait ran out
         if (named_bar_or(bar_id, 128, over || !ready || *abort_flag != 0)) {
@@ -676,18 +691,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) cnt[j] = s_count[(rbase + j) * 4 + wq];
         }
       }
-      if (aborted) break;
       if constexpr (kScores) {
-        // the pools no tile covered: -inf up to ld for each of the group's rows
+        // every warp of the group reaches this vote, including one whose wait ran out
+        if (named_bar_or(bar_id, 128, aborted)) break;
+        // the pools no tile covered: -inf up to ld for each of the group's rows, in
+        // 16-byte stores where the row allows (the next item's row state is written
+        // only after the group barrier at the top of the item loop)
         const int64_t p_from = int64_t(it.n_tiles) * kTilePools;
         for (int j = 0; j < 4; ++j) {
           const int64_t orow = int64_t(s_tau[rbase + j]);
-          if (orow >= 0)
-            for (int64_t pp = p_from + gt; pp < ld; pp += 128) __stcs(out_scores + orow * ld + pp, -INFINITY);
+          if (orow < 0) continue;
+          float* orow_p = out_scores + orow * ld;
+          int64_t pp = p_from;
+          if (pp < ld && (reinterpret_cast<uintptr_t>(orow_p + pp) & 15) == 0) {
+            const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            for (int64_t v = pp + 4 * gt; v + 4 <= ld; v += 4 * 128) __stcs(reinterpret_cast<float4*>(orow_p + v), ninf);
+            pp += (ld - pp) / 4 * 4;  // the scalar loop below writes the last (ld - p_from) % 4
+          }
+          for (int64_t v = pp + gt; v < ld; v += 128) __stcs(orow_p + v, -INFINITY);
         }
-        named_bar(bar_id, 128);  // the item's row state is read above; the next item rewrites it
         continue;
       }
+      if (aborted) break;
       if (overflow && lane == 0) record_error(hdr, KPOOL_ERR_INTERNAL);
       // final ranking: cut each of the group's rows to its top `budget` keys, dealt
       // evenly over the four regions (the group's four warps together), then warp wq
