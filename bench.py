@@ -52,13 +52,14 @@ PAGES_SEC_512K = 21.07
 # DRAM traffic of the score+select kernel from one ncu capture, per launch at the
 # pages-scale workload, tied to the kernel source it was measured on: when the
 # source hash differs the number is stale and is reported as null.
-NCU_TRAFFIC = {"kernel_sha256": "7d538d9c030732b9", "workload": "pages_512k",
-               # long_128k capture: 1.102391 GB read + 0.213307 GB written per launch; q, w and the
+NCU_TRAFFIC = {"kernel_sha256": "b2b403c7a984bacd", "workload": "pages_512k",
+               # long_128k capture: 1.101400 GB read + 0.212180 GB written per launch; q, w and the
                # pool ids grow with the rows, so x4 at 524288 tokens
-               "bytes_per_launch": 4 * (1.102391296e9 + 0.21330688e9)}
+               "bytes_per_launch": 4 * (1101400320 + 212180480)}
 # The same for the index-score mode of that kernel, per launch of the long_128k chunked run
-# (the mean over one step's chunk launches); None until captured.
-NCU_TRAFFIC_SCORES = {"kernel_sha256": None, "workload": "long_128k", "bytes_per_launch": None}
+# (the mean over one step's 8 chunk launches: 1.130 GB read, 16.669 GB written in all).
+NCU_TRAFFIC_SCORES = {"kernel_sha256": "b2b403c7a984bacd", "workload": "long_128k",
+                      "bytes_per_launch": (1129857280 + 16668774144) / 8}
 
 
 def source_sha(path: str) -> str:
