@@ -2,6 +2,7 @@
 // the ordered selection key, and the launch wrappers each .cu file provides.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -182,6 +183,11 @@ kpool_status select_check_args(const void* q, const void* kin, const float* w, c
                                const int32_t* out_pool_ids, const int32_t* out_token_ids,
                                const float* out_pool_scores, const kpool_options* options, bool* use_tc,
                                int64_t* row_begin, int64_t* row_end);
+
+// TMA descriptor of a [rows, 128] row-major bf16 matrix read in boxes of 64 columns x
+// box_rows rows with 128-byte swizzle (kpool_tmap.cu). False if the driver's encoder is
+// unavailable or rejects the arguments (base not 16-byte aligned, too many rows).
+bool make_tmap_bf16_k128(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
 
 // Bounded-wait self test.
 cudaError_t launch_wait_selftest(char* ws, int64_t spin_limit, cudaStream_t stream);

@@ -12,9 +12,9 @@
 // over many CTAs and keeps the [rows, pools] scores (a few MiB, L2-resident):
 //   R0 rows_plan_kernel   (1 CTA)   checks cu_seqlens and the rows, pool offsets,
 //                                   per-row eligible counts and the work units
-//   R1 rows_score_kernel  (grid)    each CTA a contiguous run of 128-pool units; bf16
-//                                   mma.sync tensor-core products, relu / weight /
-//                                   head sum in registers, fp32 scores out
+//   R1 rows_score_kernel  (1 CTA/SM) each CTA a contiguous run of 128-pool units:
+//                                   TMA pool tiles -> tcgen05.mma into TMEM ->
+//                                   relu / weight / head sum per pool, fp32 scores out
 //   R2 rows_collect_kernel (grid)   from a per-row histogram of the scores' top 12
 //                                   bits (built by R1) finds the bin holding the
 //                                   budget-th score, then gathers every pool above
@@ -24,15 +24,15 @@
 //                                   search over the row when the bin overflows), a
 //                                   256-thread bitonic sort, ids / scores / tokens
 // R1-R3 use programmatic dependent launch (see wait_prior_kernel below).
-// R1 streams the pooled keys once per row (HBM-bound: 256 B per pool); the
-// contraction per pool is 32 heads x 128 channels, small enough that the
-// warp-level mma.sync form keeps up with memory, so the tcgen05 pipeline of the
-// batch kernel is not needed here.
+// R1 streams the pooled keys once per row (HBM-bound: 256 B per pool, 8192 flop);
+// its job is to keep enough of them in flight, which a deep TMA ring does.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "kpool_internal.cuh"
+#include "kpool_ptx.cuh"
 #include "kpool_select_common.cuh"
 
 namespace kpool {
@@ -41,7 +41,6 @@ namespace {
 constexpr int kRowsHeads = 32;
 constexpr int kRowsDim = 128;
 constexpr int kUnitPools = 128;        // pools per work unit of R1 (the split granularity)
-constexpr int kScoreWarps = 8;         // R1: 8 warps x 16 pools per round
 constexpr int kSelectThreads = 256;    // R3 (block_sort512_desc takes exactly 256 threads)
 constexpr int kRowsMaxBudget = 512;    // R3 sorts at most 512 keys
 constexpr int kHistBits = 12;          // histogram of score_order_bits >> (32 - kHistBits)
@@ -168,142 +167,303 @@ __global__ void __launch_bounds__(256) rows_plan_kernel(const int32_t* __restric
 
 // ----------------------------------------------------------------- R1 score
 //
-// mma.sync.m16n8k16 (bf16 in, fp32 accumulate): a warp takes 16 pools (M) x 8
-// heads (N) per instruction, 4 instructions cover the 32 heads and 8 k-steps the
-// 128 channels. The channel order inside a 32-channel block is permuted the same
-// way for both operands (a dot product does not depend on it), so every thread
-// fills its fragments from 16-byte loads: thread (g = lane / 4, c = lane % 4)
-// reads channels 32m + 8c .. 32m + 8c + 7 of pools g and g + 8 and of heads
-// g + 8n. The first four of those eight channels feed k-step 2m, the last four
-// k-step 2m + 1.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// Per work unit (128 pools of one row) the TMA producer (warp 0) loads the
+// [128 pools x 128] bf16 pooled-key tile (32 KB, 128-byte swizzle) into a 6-stage
+// ring and, when the row changes, the row's [32 heads x 128] query tile. The MMA
+// issuer (warp 1, owner of 128 TMEM columns) multiplies them as 8 tcgen05.mma
+// (M = 128 pools, N = 32 heads, K = 16 each) into one of four 32-column fp32
+// accumulators. Four epilogue warps (warp w reads TMEM lanes 32 (w % 4) ..) take one
+// pool per thread: its 32 head products come in with one tcgen05.ld, then relu,
+// |scale| and the head weights and the head sum, in the score kernel's arithmetic
+// (x + |x| against halved weights, packed fp32 FMAs, pairs summed last), the score is
+// stored and its top bits counted in the CTA's histogram of the row, which is added
+// to the row's global histogram when the row ends. Every mbarrier wait is bounded;
+// a wait that runs out records KPOOL_ERR_DEVICE_TIMEOUT and every role winds down.
+namespace r1 {
+constexpr int kThreads = 192;                                // producer, MMA issuer, 4 epilogue warps
+constexpr int kStages = 6;                                   // pool tiles in flight
+constexpr int kAccs = 4;                                     // TMEM accumulators
+constexpr int kAccCols = kRowsHeads;                         // 32 fp32 columns each
+constexpr int kTmemCols = kAccs * kAccCols;                  // 128 (a power of two >= 32)
+constexpr uint32_t kPoolHalf = kUnitPools * 128;             // 128 pools x 64 bf16
+constexpr uint32_t kStageBytes = 2 * kPoolHalf;              // 32 KB
+constexpr uint32_t kQHalf = kRowsHeads * 128;                // 32 heads x 64 bf16
+constexpr uint32_t kQBytes = 2 * kQHalf;                     // 8 KB
+constexpr uint32_t kOffPool = 0;
+constexpr uint32_t kOffQ = kOffPool + kStages * kStageBytes;  // 1024-byte aligned
+constexpr uint32_t kOffHist = kOffQ + kQBytes;
+constexpr uint32_t kOffBar = kOffHist + kHistBins * 4;
+constexpr int kNumBars = 2 * kStages + 2 * kAccs + 3;        // full, empty, acc_full, acc_empty, q_full, q_empty, mma_done
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;        // TMEM base, abort flag
+constexpr uint32_t kSmemBytes = kOffMisc + 16;
+static_assert(kOffQ % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+constexpr int64_t kMaxPolls = int64_t(1) << 40;
+constexpr uint64_t kMaxWaitNs = 1000000000ull;  // 1 s; legitimate waits are microseconds
+constexpr int kEpiBar = 1;                       // named barrier of the 4 epilogue warps
+constexpr int kEndBar = 2;                       // named barrier of the whole CTA at teardown
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-__global__ void __launch_bounds__(kScoreWarps * 32) rows_score_kernel(
-    const uint4* __restrict__ q, const float* __restrict__ w, const uint4* __restrict__ kp,
-    const RowInfo* __restrict__ info, const int32_t* __restrict__ unit_off, const WorkspaceHeader* hdr, int R,
-    float scale, float* __restrict__ scores, int64_t stride, uint32_t* __restrict__ hist) {
-  __shared__ uint32_t s_hist[kHistBins];  // this unit's histogram, flushed to the row's at the end
-  __shared__ uint4 s_q[16][32];           // the row's query fragments (see below)
-  wait_prior_kernel();  // the plan: n_items, row records, unit offsets (and the cleared histograms)
+// Row of unit u: the last r with unit_off[r] <= u (rows without units are skipped).
+__device__ __forceinline__ int row_of_unit(const int32_t* unit_off, int R, int u) {
+  int lo = 0, hi = R - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(unit_off + mid) <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+}  // namespace r1
+
+__global__ void __launch_bounds__(r1::kThreads, 1) rows_score_kernel(
+    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
+    const float* __restrict__ w, const RowInfo* __restrict__ info, const int32_t* __restrict__ unit_off,
+    WorkspaceHeader* __restrict__ hdr, int R, float scale, float* __restrict__ scores, int64_t stride,
+    uint32_t* __restrict__ hist) {
+  using namespace r1;
+  extern __shared__ __align__(1024) uint8_t smem[];
   allow_next_kernel();
-  const int n_units = hdr->n_items;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const float abs_scale = fabsf(scale);
-  const bool neg = scale < 0.0f;
-  constexpr int kVecPerRow = kRowsDim / 8;  // 16-byte vectors per pooled key / query head
-  // this CTA's share: a contiguous run of units, i.e. one or a few contiguous pool
-  // ranges ("segments") of consecutive rows
+  // a uniform exit, before any barrier or TMEM allocation (the error word is written
+  // only after the planning kernel, which resets it, has finished)
+  if ((ptx::smem_addr(smem) & 1023u) != 0) {
+    wait_prior_kernel();
+    if (threadIdx.x == 0) record_error(hdr, KPOOL_ERR_INTERNAL);
+    return;
+  }
+  // the set-up below reads nothing the planning kernel writes, so it runs while that
+  // kernel finishes (programmatic dependent launch)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + kAccs;
+  uint64_t* q_full = acc_empty + kAccs;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* mma_done = q_empty + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + kOffMisc + 4);
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      ptx::mbar_init(full + i, 1);
+      ptx::mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < kAccs; ++i) {
+      ptx::mbar_init(acc_full + i, 1);
+      ptx::mbar_init(acc_empty + i, 4);  // one arrival per epilogue warp
+    }
+    ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
+    ptx::mbar_init(mma_done, 1);
+    ptx::fence_mbar_init();
+    *abort_flag = 0;
+    ptx::prefetch_tmap(&tmap_q);
+    ptx::prefetch_tmap(&tmap_kp);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(s_tmem, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i < kHistBins; i += kThreads) s_hist[i] = 0;
+  wait_prior_kernel();  // the plan: n_items, row records, unit offsets (and the cleared histograms)
+  const int n_units = hdr->n_items;  // 0 when the plan found cu_seqlens malformed
   const int u_first = int(int64_t(n_units) * blockIdx.x / gridDim.x);
   const int u_last = int(int64_t(n_units) * (blockIdx.x + 1) / gridDim.x);
-  for (int u = u_first; u < u_last;) {
-    // row of unit u: the last r with unit_off[r] <= u
-    int lo = 0, hi = R - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(unit_off + mid) <= u) lo = mid; else hi = mid - 1;
-    }
-    const int r = lo;
-    const RowInfo ri = info[r];
-    const int seg_end = min(u_last, __ldg(unit_off + r + 1));
-    const int p_begin = (u - unit_off[r]) * kUnitPools;
-    const int e = ri.e;
-    const int p_end = min(e, (seg_end - unit_off[r]) * kUnitPools);
-    u = seg_end;
-    // query fragments of all 32 heads, one copy per lane slot in shared memory so the
-    // registers stay free for a second set of pooled-key loads in flight:
-    // s_q[n * 4 + m][lane] holds channels 32m + 8c .. + 7 of head g + 8n
-    __syncthreads();  // the previous unit's fragments are no longer read
-    for (int i = threadIdx.x; i < 16 * 32; i += blockDim.x) {
-      const int f = i >> 5, l = i & 31, n = f >> 2, m = f & 3;
-      s_q[f][l] = __ldg(q + (int64_t(r) * kRowsHeads + (l >> 2) + 8 * n) * kVecPerRow + 4 * m + (l & 3));
-    }
-    // this thread's accumulator columns are heads 8n + 2c and 8n + 2c + 1
-    float wt[4][2];
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      wt[n][0] = __ldg(w + int64_t(r) * kRowsHeads + 8 * n + 2 * c) * abs_scale;
-      wt[n][1] = __ldg(w + int64_t(r) * kRowsHeads + 8 * n + 2 * c + 1) * abs_scale;
-    }
-    float* out = scores + int64_t(r) * stride;
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) s_hist[i] = 0;
-    __syncthreads();
-    // pooled keys of pools p + g and p + g + 8, clamped to an eligible pool (the scores
-    // of clamped rows are not stored); the next 16 pools load while these are scored
-    auto load_keys = [&](int p, uint4 (&ka)[4], uint4 (&kb)[4]) {
-      const int pa = min(p + g, e - 1), pb = min(p + g + 8, e - 1);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        ka[m] = __ldg(kp + int64_t(ri.pool_base + pa) * kVecPerRow + 4 * m + c);
-        kb[m] = __ldg(kp + int64_t(ri.pool_base + pb) * kVecPerRow + 4 * m + c);
-      }
-    };
-    uint4 ka[4], kb[4], na[4], nb[4];
-    int p0 = p_begin + warp * 16;
-    if (p0 < p_end) load_keys(p0, ka, kb);
-    for (; p0 < p_end; p0 += kScoreWarps * 16) {
-      const int pn = p0 + kScoreWarps * 16;
-      if (pn < p_end) load_keys(pn, na, nb);
-      float acc[4][4];
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[n][i] = 0.0f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const uint32_t a_lo[4] = {ka[m].x, kb[m].x, ka[m].y, kb[m].y};  // k-step 2m
-        const uint32_t a_hi[4] = {ka[m].z, kb[m].z, ka[m].w, kb[m].w};  // k-step 2m + 1
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          const uint4 qf = s_q[n * 4 + m][lane];
-          mma_bf16_16816(acc[n], a_lo, qf.x, qf.y);
-          mma_bf16_16816(acc[n], a_hi, qf.z, qf.w);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  if (u_first >= u_last) {
+    // no units for this CTA: straight to the teardown (TMEM is still freed there)
+  } else if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------------------- producer
+      const uint64_t pol = ptx::policy_evict_first();  // every key tile is read once
+      int stage = 0, r = row_of_unit(unit_off, R, u_first), cur = -1;
+      uint32_t phase = 0, fills = 0, q_loads = 0;
+      bool ok = true;
+      for (int u = u_first; u < u_last; ++u) {
+        while (__ldg(unit_off + r + 1) <= u) ++r;
+        if (r != cur) {  // the row's query tile, once the previous row's MMAs are done with it
+          if (q_loads > 0 && !ptx::mbar_wait_bounded(q_empty, (q_loads - 1) & 1, kMaxPolls, kMaxWaitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(q_full, kQBytes);
+          ptx::tma_load_2d_hint(smem + kOffQ, &tmap_q, q_full, 0, r * kRowsHeads, pol);
+          ptx::tma_load_2d_hint(smem + kOffQ + kQHalf, &tmap_q, q_full, 64, r * kRowsHeads, pol);
+          ++q_loads;
+          cur = r;
+        }
+        if (!ptx::mbar_wait_bounded(empty + stage, phase ^ 1, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        const int32_t prow = info[r].pool_base + (u - __ldg(unit_off + r)) * kUnitPools;
+        uint8_t* dst = smem + kOffPool + stage * kStageBytes;
+        ptx::mbar_arrive_expect_tx(full + stage, kStageBytes);
+        ptx::tma_load_2d_hint(dst, &tmap_kp, full + stage, 0, prow, pol);
+        ptx::tma_load_2d_hint(dst + kPoolHalf, &tmap_kp, full + stage, 64, prow, pol);
+        ++fills;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        ka[m] = na[m];
-        kb[m] = nb[m];
+      if (!ok) {
+        record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
       }
-      // acc[n][0..1]: pool g, heads 8n + 2c, +1; acc[n][2..3]: pool g + 8
-      float sa = 0.0f, sb = 0.0f;
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        sa = fmaf(wt[n][0], fmaxf(neg ? -acc[n][0] : acc[n][0], 0.0f), sa);
-        sa = fmaf(wt[n][1], fmaxf(neg ? -acc[n][1] : acc[n][1], 0.0f), sa);
-        sb = fmaf(wt[n][0], fmaxf(neg ? -acc[n][2] : acc[n][2], 0.0f), sb);
-        sb = fmaf(wt[n][1], fmaxf(neg ? -acc[n][3] : acc[n][3], 0.0f), sb);
+      // every copy armed above lands before the CTA exits
+      for (int s2 = 0; s2 < kStages; ++s2) {
+        const uint32_t armed = (fills + kStages - 1 - s2) / kStages;
+        if (armed) ptx::mbar_wait_bounded(full + s2, (armed - 1) & 1, kMaxPolls, kMaxWaitNs);
       }
-      // head sum across the four threads of a pool
-      sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-      sa += __shfl_xor_sync(0xffffffffu, sa, 2);
-      sb += __shfl_xor_sync(0xffffffffu, sb, 1);
-      sb += __shfl_xor_sync(0xffffffffu, sb, 2);
-      const int pm = c == 0 ? p0 + g : p0 + g + 8;
-      const float sm = c == 0 ? sa : sb;
-      const bool has = c < 2 && pm < e;
-      if (has) out[pm] = sm;
-      // histogram of the top bits, one shared atomic per distinct bin in the warp
-      const uint32_t bin = score_order_bits(sm) >> (32 - kHistBits);
-      const unsigned act = __ballot_sync(0xffffffffu, has);
-      if (has) {
-        const unsigned peers = __match_any_sync(act, bin);
-        if ((__ffs(peers) - 1) == lane) atomicAdd(s_hist + bin, uint32_t(__popc(peers)));
+      if (q_loads) ptx::mbar_wait_bounded(q_full, (q_loads - 1) & 1, kMaxPolls, kMaxWaitNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------------------------ MMA
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kUnitPools, kRowsHeads);
+      const uint32_t pool_addr = ptx::smem_addr(smem + kOffPool), q_addr = ptx::smem_addr(smem + kOffQ);
+      int stage = 0, acc = 0, r = row_of_unit(unit_off, R, u_first), cur = -1;
+      uint32_t phase = 0, acc_phase = 0, q_uses = 0;
+      bool ok = true;
+      for (int u = u_first; u < u_last; ++u) {
+        while (__ldg(unit_off + r + 1) <= u) ++r;
+        if (r != cur) {
+          if (!ptx::mbar_wait_bounded(q_full, q_uses & 1, kMaxPolls, kMaxWaitNs)) {
+            ok = false;
+            break;
+          }
+          ++q_uses;
+          cur = r;
+        }
+        if (!ptx::mbar_wait_bounded(acc_empty + acc, acc_phase ^ 1, kMaxPolls, kMaxWaitNs) ||
+            !ptx::mbar_wait_bounded(full + stage, phase, kMaxPolls, kMaxWaitNs) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t a_base = pool_addr + stage * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t a_addr = a_base + (kk >> 2) * kPoolHalf + (kk & 3) * 32;
+          const uint32_t b_addr = q_addr + (kk >> 2) * kQHalf + (kk & 3) * 32;
+          ptx::tc_mma_f16(tmem_base + uint32_t(acc * kAccCols), ptx::smem_desc_kmajor_sw128(a_addr),
+                          ptx::smem_desc_kmajor_sw128(b_addr), idesc, kk > 0 ? 1u : 0u);
+        }
+        ptx::tc_commit(empty + stage);
+        ptx::tc_commit(acc_full + acc);
+        if (u + 1 == u_last || __ldg(unit_off + r + 1) <= u + 1) ptx::tc_commit(q_empty);  // row's last unit
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++acc == kAccs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (!ok) {
+        record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      ptx::tc_commit(mma_done);  // every MMA issued above completes before TMEM is freed
+      ptx::mbar_wait_bounded(mma_done, 0, kMaxPolls, kMaxWaitNs);
+    }
+  } else {  // ---------------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64;  // 0..127
+    const int lq = warp & 3;          // TMEM lane quarter this warp may read
+    const uint32_t lane_addr = tmem_base + (uint32_t(lq * 32) << 16);
+    const float abs_scale = fabsf(scale);
+    const bool neg = scale < 0.0f;
+    int acc = 0, r = row_of_unit(unit_off, R, u_first), cur = -1;
+    uint32_t acc_phase = 0;
+    uint64_t wp[kRowsHeads / 2];  // halved |scale| w of head pairs
+    RowInfo ri{};
+    auto flush_hist = [&](int row) {  // the CTA's counts of `row` into the row's histogram
+      named_bar(kEpiBar, 128);
+      uint32_t* h = hist + int64_t(row) * kHistBins;
+      for (int i = et; i < kHistBins; i += 128) {
+        const uint32_t v = s_hist[i];
+        if (v) {
+          atomicAdd(h + i, v);
+          s_hist[i] = 0;
+        }
+      }
+      named_bar(kEpiBar, 128);
+    };
+    for (int u = u_first; u < u_last; ++u) {
+      while (__ldg(unit_off + r + 1) <= u) ++r;
+      if (r != cur) {
+        if (cur >= 0) flush_hist(cur);
+        ri = info[r];
+#pragma unroll
+        for (int h2 = 0; h2 < kRowsHeads / 2; ++h2)
+          wp[h2] = ptx::pack_f32x2((__ldg(w + int64_t(r) * kRowsHeads + 2 * h2) * abs_scale) * 0.5f,
+                                   (__ldg(w + int64_t(r) * kRowsHeads + 2 * h2 + 1) * abs_scale) * 0.5f);
+        cur = r;
+      }
+      // every lane tests the barrier; after an abort the units are only counted off
+      const bool ready = *abort_flag == 0 &&
+                         __all_sync(0xffffffffu, ptx::mbar_wait_bounded(acc_full + acc, acc_phase, kMaxPolls,
+                                                                        kMaxWaitNs));
+      if (ready) {
+        ptx::tc_fence_after();
+        uint32_t v[32];
+        ptx::tc_ld_32x32b_x32(lane_addr + uint32_t(acc * kAccCols), v);
+        ptx::tc_wait_ld();
+        ptx::tc_reg_fence(v);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(acc_empty + acc);
+        uint64_t a0 = 0, a1 = 0;
+#pragma unroll
+        for (int h4 = 0; h4 < kRowsHeads / 4; ++h4) {
+          const float x0 = __uint_as_float(v[4 * h4 + 0]), x1 = __uint_as_float(v[4 * h4 + 1]);
+          const float x2 = __uint_as_float(v[4 * h4 + 2]), x3 = __uint_as_float(v[4 * h4 + 3]);
+          // x + |x| = 2 relu(x) exactly (|x| - x for a negative scale) against halved weights
+          a0 = ptx::fma_f32x2(wp[2 * h4], ptx::pack_f32x2(neg ? fabsf(x0) - x0 : x0 + fabsf(x0),
+                                                          neg ? fabsf(x1) - x1 : x1 + fabsf(x1)), a0);
+          a1 = ptx::fma_f32x2(wp[2 * h4 + 1], ptx::pack_f32x2(neg ? fabsf(x2) - x2 : x2 + fabsf(x2),
+                                                              neg ? fabsf(x3) - x3 : x3 + fabsf(x3)), a1);
+        }
+        float s0, s1, s2, s3;
+        ptx::unpack_f32x2(a0, s0, s1);
+        ptx::unpack_f32x2(a1, s2, s3);
+        const float sc = (s0 + s1) + (s2 + s3);
+        const int p = (u - __ldg(unit_off + r)) * kUnitPools + lq * 32 + lane;
+        const bool has = p < ri.e;
+        if (has) scores[int64_t(r) * stride + p] = sc;
+        // histogram of the top bits, one shared atomic per distinct bin in the warp
+        const uint32_t bin = score_order_bits(sc) >> (32 - kHistBits);
+        const unsigned act = __ballot_sync(0xffffffffu, has);
+        if (has) {
+          const unsigned peers = __match_any_sync(act, bin);
+          if ((__ffs(peers) - 1) == lane) atomicAdd(s_hist + bin, uint32_t(__popc(peers)));
+        }
+      } else if (lane == 0 && *abort_flag == 0) {
+        record_error(hdr, KPOOL_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (++acc == kAccs) {
+        acc = 0;
+        acc_phase ^= 1;
       }
     }
-    __syncthreads();
-    uint32_t* h = hist + int64_t(r) * kHistBins;
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
-      const uint32_t v = s_hist[i];
-      if (v) atomicAdd(h + i, v);
-    }
-    __syncthreads();
+    if (cur >= 0) flush_hist(cur);
+    ptx::tc_fence_before();
+  }
+  // ---------------------------------------------------------------------- teardown
+  __syncwarp();
+  named_bar(kEndBar, kThreads);
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -622,11 +782,12 @@ namespace {
 // previous kernel on the stream runs and waits for it in wait_prior_kernel().
 // Captured into a graph, the dependency becomes a programmatic edge.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_after_prior(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+cudaError_t launch_after_prior(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -691,23 +852,37 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
   e = cudaGetLastError();
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return e;
-  // units: at most R * ceil(max pools / kUnitPools); one wave of 2 CTAs per SM splits them
+  // units: at most R * ceil(max pools / kUnitPools); one persistent CTA per SM splits them
   const int64_t max_units = int64_t(R) * ((L.stride + kUnitPools - 1) / kUnitPools);
-  int grid = int(max_units < int64_t(2) * num_sms ? (max_units > 0 ? max_units : 1) : int64_t(2) * num_sms);
+  int grid = int(max_units < num_sms ? (max_units > 0 ? max_units : 1) : num_sms);
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
-  e = launch_after_prior(rows_score_kernel, dim3(grid), dim3(kScoreWarps * 32), stream, static_cast<const uint4*>(q),
-                         w, static_cast<const uint4*>(kp), static_cast<const RowInfo*>(info),
-                         static_cast<const int32_t*>(unit_off), static_cast<const WorkspaceHeader*>(hdr), R, scale,
-                         scores, L.stride, hist);
+  // no pooled keys (T / kpool == 0): every row has no eligible pool and no unit to score
+  if (kp != nullptr && T / kpool > 0) {
+    CUtensorMap map_q, map_kp;
+    if (!make_tmap_bf16_k128(&map_q, q, uint64_t(R) * kRowsHeads, kRowsHeads) ||
+        !make_tmap_bf16_k128(&map_kp, kp, uint64_t(T / kpool), kUnitPools))
+      return cudaErrorInvalidValue;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && (dev < 0 || dev >= 64 || !attr_set[dev])) {
+      e = cudaFuncSetAttribute(rows_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(r1::kSmemBytes));
+      if (e == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    if (e != cudaSuccess) return e;
+    e = launch_after_prior(rows_score_kernel, dim3(grid), dim3(r1::kThreads), r1::kSmemBytes, stream, map_q, map_kp,
+                           w, static_cast<const RowInfo*>(info), static_cast<const int32_t*>(unit_off), hdr, R, scale,
+                           scores, L.stride, hist);
+  }
   if (e == cudaSuccess) e = mark(2);
   if (e != cudaSuccess) return e;
   const int64_t slices = (L.stride + kCollectPools - 1) / kCollectPools;
   const dim3 cgrid(unsigned(slices < kCollectCtasPerRow ? slices : kCollectCtasPerRow), unsigned(R));
-  e = launch_after_prior(rows_collect_kernel, cgrid, dim3(kCollectThreads), stream, static_cast<const float*>(scores),
+  e = launch_after_prior(rows_collect_kernel, cgrid, dim3(kCollectThreads), 0, stream, static_cast<const float*>(scores),
                          L.stride, static_cast<const RowInfo*>(info), static_cast<const WorkspaceHeader*>(hdr), budget,
                          static_cast<const uint32_t*>(hist), cand_cnt, cand, tie_cnt, ties);
   if (e != cudaSuccess) return e;
-  e = launch_after_prior(rows_select_kernel, dim3(R), dim3(kSelectThreads), stream, static_cast<const float*>(scores),
+  e = launch_after_prior(rows_select_kernel, dim3(R), dim3(kSelectThreads), 0, stream, static_cast<const float*>(scores),
                          L.stride, static_cast<const RowInfo*>(info), static_cast<const WorkspaceHeader*>(hdr), kpool,
                          budget, static_cast<const int32_t*>(cand_cnt), static_cast<const uint64_t*>(cand),
                          static_cast<const int32_t*>(tie_cnt), static_cast<const uint64_t*>(ties), out_ids, out_scores,

@@ -758,37 +758,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// 2-D bf16 map over a [rows, 128] row-major matrix, box = 64 columns x box_rows,
-// 128-byte swizzle (the layout the MMA descriptors above expect).
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(kDim) * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool g_attr_set[64][4] = {};
 
 }  // namespace
@@ -806,9 +775,9 @@ cudaError_t launch_tc(bool scores, const void* q, const void* kp, const float* w
   if (T == 0 || row_end <= row_begin) return cudaSuccess;
   if (T * kHeads > int64_t(INT32_MAX)) return cudaErrorInvalidValue;
   CUtensorMap map_q, map_kp;
-  if (!make_map(&map_q, q, uint64_t(T) * kHeads, kN)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_k128(&map_q, q, uint64_t(T) * kHeads, kN)) return cudaErrorInvalidValue;
   const uint64_t kp_rows = L.max_pools > 0 ? uint64_t(L.max_pools) : 1;
-  if (!make_map(&map_kp, kp, kp_rows, kTilePools)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_k128(&map_kp, kp, kp_rows, kTilePools)) return cudaErrorInvalidValue;
   const bool neg = scale < 0.0f;
   const float abs_scale = neg ? -scale : scale;
   auto kern = scores ? (neg ? select_tc_kernel<true, true> : select_tc_kernel<false, true>)

@@ -94,6 +94,28 @@ def test_rows_equal_batch_rows_on_integer_data():
     np.testing.assert_array_equal(toks, tok_all[rows.cuda()].cpu().numpy())
 
 
+def test_rows_equal_batch_rows_on_float_data():
+    """Both score kernels run the same tcgen05 contraction (K = 128 in the same eight K = 16
+    steps) and the same fp32 epilogue, so decode rows reproduce the batch selection bit for
+    bit on float data too: ids, tokens and scores."""
+    wl = W.custom("pickf", (3000, 17, 2100), 32, 128, 4, 2048, 1.0 / np.sqrt(128), "bf16", "normal", 31)
+    inp = {k: v.cuda() for k, v in W.generate(wl, "cpu").items()}
+    ids_all, tok_all, sc_all = K.kpool_select_ex(inp["q"], inp["k"], inp["w"], inp["cu_seqlens"], wl.kpool,
+                                                 wl.index_topk, wl.scale, return_scores=True,
+                                                 score_kernel=K.KPOOL_SCORE_TC)
+    rows = torch.arange(0, wl.total_tokens, 7)
+    cu = inp["cu_seqlens"].cpu()
+    b = torch.searchsorted(cu, rows, right=True) - 1
+    kp = K.kpool_pool_keys(inp["k"], inp["cu_seqlens"], wl.kpool)
+    ids, toks, sc = K.kpool_select_rows(inp["q"][rows.cuda()].contiguous(), inp["w"][rows.cuda()].contiguous(),
+                                        b.to(torch.int32).cuda(), (rows - cu[b]).to(torch.int32).cuda(), kp,
+                                        inp["cu_seqlens"], wl.total_tokens, wl.kpool, wl.index_topk, wl.scale,
+                                        return_scores=True)
+    torch.cuda.synchronize()
+    r = rows.cuda()
+    assert torch.equal(ids, ids_all[r]) and torch.equal(toks, tok_all[r]) and torch.equal(sc, sc_all[r])
+
+
 def test_rows_invalid_rows_are_empty_and_reported():
     wl = W.DECODE_TIE
     inp = W.generate_rows(wl, "cuda")
