@@ -52,14 +52,18 @@ PAGES_SEC_512K = 21.07
 # DRAM traffic of the score+select kernel from one ncu capture, per launch at the
 # pages-scale workload, tied to the kernel source it was measured on: when the
 # source hash differs the number is stale and is reported as null.
-NCU_TRAFFIC = {"kernel_sha256": "b2b403c7a984bacd", "workload": "pages_512k",
-               # long_128k capture: 1.101400 GB read + 0.212180 GB written per launch; q, w and the
+NCU_TRAFFIC = {"kernel_sha256": "8c12fac7b912701f", "workload": "pages_512k",
+               # long_128k capture: 1.100543 GB read + 0.212087 GB written per launch; q, w and the
                # pool ids grow with the rows, so x4 at 524288 tokens
-               "bytes_per_launch": 4 * (1101400320 + 212180480)}
+               "bytes_per_launch": 4 * (1100542976 + 212086784)}
 # The same for the index-score mode of that kernel, per launch of the long_128k chunked run
-# (the mean over one step's 8 chunk launches: 1.130 GB read, 16.669 GB written in all).
-NCU_TRAFFIC_SCORES = {"kernel_sha256": "b2b403c7a984bacd", "workload": "long_128k",
-                      "bytes_per_launch": (1129857280 + 16668774144) / 8}
+# (the mean over one step's 8 chunk launches: 1.130 GB read, 16.668 GB written in all).
+NCU_TRAFFIC_SCORES = {"kernel_sha256": "8c12fac7b912701f", "workload": "long_128k",
+                      "bytes_per_launch": (1129766656 + 16667923712) / 8}
+# And for the decode rows' score kernel (kpool_rows.cu), per launch at decode_262k (the mean
+# over three launches).
+NCU_TRAFFIC_ROWS = {"kernel_sha256": "f11a8d227c3d7e15", "workload": "decode_262k",
+                    "bytes_per_launch": (806034432 + 8933888) / 3}
 
 
 def source_sha(path: str) -> str:
@@ -255,6 +259,14 @@ def reference_arm(args, wl, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def rows_traffic(wl) -> float | None:
+    """DRAM bytes per launch of the decode score kernel from the ncu capture, while the
+    kernel source is the one that was captured and the workload the captured one."""
+    src = os.path.join(ROOT, "sparse_attention_kpool_gb300", "csrc", "kpool_rows.cu")
+    t = NCU_TRAFFIC_ROWS
+    return t["bytes_per_launch"] if t["kernel_sha256"] == source_sha(src) and t["workload"] == wl.name else None
+
+
 def rows_config(wl: W.RowsWorkload, world: int) -> dict:
     return {"workload": wl.name, "key_seqlens": list(wl.seqlens) if len(set(wl.seqlens)) > 1 else
             f"{len(wl.seqlens)} x {wl.seqlens[0]}", "rows": wl.num_rows, "heads": wl.heads,
@@ -431,7 +443,7 @@ def rows_bench(args, wl: W.RowsWorkload, world: int, rank: int, emit: bool = Tru
                       "timed": "graph replay" if k_ms_graph is not None else "eager"},
         "kernel_ms_eager": {"plan": k_ms_eager[0], "score": k_ms_eager[1], "select": k_ms_eager[2]},
         "roofline": {"kernel": "rows_score_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": rows_traffic(wl),
                      "peak_kind": f"HBM copy, {peaks['_source']}", "algorithmic_bytes_per_launch": score_bytes},
         "clocks": clock_info, "gpu_launches": 4 * args.steps,
         "e2e": {"value": world * pairs / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
