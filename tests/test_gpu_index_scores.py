@@ -136,6 +136,19 @@ def test_chunks_concatenate_to_the_whole_call():
         assert torch.equal(torch.cat(parts), whole), f"bounds {bounds}"
 
 
+@pytest.mark.parametrize("max_ctas", [1, 7, 152])
+def test_any_grid_gives_the_same_scores(max_ctas):
+    """The persistent kernel's CTAs take work items from a counter: one CTA working
+    through every item, or a few, must write the same matrix as the full grid."""
+    wl = _wl("normal", 101, seqlens=(1900, 3, 700))
+    dev = to_dev(W.generate(wl, "cpu"))
+    ld = wl.total_tokens // wl.kpool
+    for kernel in (TC, SIMT):
+        ref = scores(dev, wl, ld=ld, score_kernel=kernel)
+        got = scores(dev, wl, ld=ld, score_kernel=kernel, max_ctas=max_ctas)
+        assert torch.equal(got, ref), f"kernel {kernel}, max_ctas {max_ctas}"
+
+
 def test_chunk_writes_only_its_rows_and_columns():
     """A chunk written into the middle of a larger buffer: the canaries on both sides survive."""
     wl = _wl("integer", 98, seqlens=(900, 500))
