@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(kCollectThreads) rows_collect_kernel(
   }
 }
 
-// ---------------------------------------------------------------- R2 select
+// ---------------------------------------------------------------- R3 select
 //
 // Exact top-budget of one row's scores. The order is that of the 64-bit
 // selection key (order-preserving score bits, then the complemented pool
