@@ -85,6 +85,20 @@ def test_simt_shapes_match_the_oracle(wl):
     parity.compare_full_scores(full, ref, exact=False, what=wl.name)
 
 
+@pytest.mark.parametrize("kpool", [1, 3, 8])
+def test_other_kpool_exact(kpool):
+    """Pools of 1, 3 and 8 keys (ragged tails, a sequence shorter than one pool): both
+    kernel families against the oracle, bit for bit on integer-valued inputs."""
+    wl = W.custom("isc_k", (777, 5, 2, 1300), 32, 128, kpool, 8 * kpool, 1.0 / 16, "bf16", "integer", 100 + kpool)
+    dev = to_dev(W.generate(wl, "cpu"))
+    ld = max(int(L) // kpool for L in wl.seqlens)
+    rows = np.arange(wl.total_tokens)
+    ref = parity.oracle_full_scores(dev, wl, rows, ld)
+    for kernel in (TC, SIMT):
+        full = scores(dev, wl, ld=ld, score_kernel=kernel).cpu().numpy()
+        parity.compare_full_scores(full, ref, exact=True, what=f"kpool {kpool}, kernel {kernel}")
+
+
 def test_negative_scale():
     wl = W.custom("isc_neg", (1500, 260), 32, 128, 4, 256, -1.0 / 16, "bf16", "integer", 95)
     dev = to_dev(W.generate(wl, "cpu"))
