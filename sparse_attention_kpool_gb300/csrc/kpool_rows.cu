@@ -97,15 +97,26 @@ __device__ int block_exclusive_scan(int v, int* total, int* s_warp) {
 }
 
 // ------------------------------------------------------------------ R0 plan
+// CTA 0 plans; CTAs 1.. clear the histograms and gather counters (`clear`, n_clear
+// 32-bit words, 16-byte aligned) that R1 and R2 accumulate into.
 __global__ void __launch_bounds__(256) rows_plan_kernel(const int32_t* __restrict__ cu, int S, int64_t T,
                                                          const int32_t* __restrict__ row_seq,
                                                          const int32_t* __restrict__ row_pos, int R, int kpool,
                                                          WorkspaceHeader* hdr, int32_t* pool_off, RowInfo* info,
-                                                         int32_t* unit_off) {
+                                                         int32_t* unit_off, uint32_t* __restrict__ clear,
+                                                         int64_t n_clear) {
   __shared__ int s_bad, s_bad_row;
   __shared__ int s_warp[32];
   const int tid = threadIdx.x;
   allow_next_kernel();
+  if (blockIdx.x > 0) {
+    const int64_t n4 = n_clear / 4;
+    const int64_t stride = int64_t(gridDim.x - 1) * blockDim.x;
+    uint4* c4 = reinterpret_cast<uint4*>(clear);
+    for (int64_t i = int64_t(blockIdx.x - 1) * blockDim.x + tid; i < n4; i += stride) c4[i] = make_uint4(0, 0, 0, 0);
+    for (int64_t i = 4 * n4 + int64_t(blockIdx.x - 1) * blockDim.x + tid; i < n_clear; i += stride) clear[i] = 0;
+    return;
+  }
   if (tid == 0) {
     s_bad = (cu[0] != 0 || int64_t(cu[S]) != T) ? 1 : 0;
     s_bad_row = 0;
@@ -846,9 +857,13 @@ cudaError_t launch_select_rows(const void* q, const float* w, const int32_t* row
                                    : record_stage_event(stage_events[i], stream);
   };
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.hist, 0, L.cleared_bytes, stream);
   if (e != cudaSuccess) return e;
-  rows_plan_kernel<<<1, 256, 0, stream>>>(cu, S, T, row_seq, row_pos, R, kpool, hdr, pool_off, info, unit_off);
+  // one planning CTA, and enough clearing CTAs that each clears about 32 KB
+  const int64_t clear_ctas = (int64_t(L.cleared_bytes) + 32767) / 32768;
+  const unsigned plan_grid = unsigned(1 + (clear_ctas < 2 * num_sms ? clear_ctas : 2 * num_sms));
+  rows_plan_kernel<<<plan_grid, 256, 0, stream>>>(cu, S, T, row_seq, row_pos, R, kpool, hdr, pool_off, info,
+                                                   unit_off, reinterpret_cast<uint32_t*>(ws + L.hist),
+                                                   int64_t(L.cleared_bytes / 4));
   e = cudaGetLastError();
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return e;
